@@ -1,0 +1,204 @@
+"""GB300 (sm_103a) exact tiled attention: Python binding of libfa.so.
+
+The functions with ``fa_`` names are one-to-one ctypes wrappers of the C ABI in
+``include/fa.h`` (raw pointers and sizes).  ``forward`` / ``backward`` marshal
+torch tensors into those calls; every step of the computation runs in the CUDA
+kernels of libfa.so.  torch supplies only device memory and the current stream.
+There is no fallback: if libfa.so is missing or fails to load, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libfa.so")
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = 1
+FA_ERR_UNSUPPORTED = 2
+FA_ERR_MISALIGNED = 3
+FA_ERR_WORKSPACE = 4
+FA_ERR_CUDA = 5
+FA_ERR_DEVICE_TIMEOUT = 6
+
+EXPORTED = (
+    "fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_bwd_prep", "fa_bwd_main",
+    "fa_bwd_finish", "fa_sync_status", "fa_status_string", "fa_version",
+)
+
+_lib = None
+
+
+class FAError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what} failed: {status_string(code)} ({code})")
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libfa.so and declare the C signatures.  Raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"libfa.so not found at {path}; build it with "
+            "`python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(path)
+    P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    sig = {
+        "fa_fwd": ([P, P, P, P, P, I, I, I, I, F, I, P], I),
+        "fa_bwd_workspace_size": ([I, I, I, I], Z),
+        "fa_bwd": ([P, P, P, P, P, P, P, P, P, I, I, I, I, F, I, P, Z, P], I),
+        "fa_bwd_prep": ([P, P, I, I, I, I, P, Z, P], I),
+        "fa_bwd_main": ([P, P, P, P, P, P, P, I, I, I, I, F, I, P, Z, P], I),
+        "fa_bwd_finish": ([P, I, I, I, I, P, Z, P], I),
+        "fa_sync_status": ([P], I),
+        "fa_status_string": ([I], ctypes.c_char_p),
+        "fa_version": ([], I),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib = lib
+    return lib
+
+
+# ---------------------------------------------------------------------------
+# one-to-one wrappers of the C ABI (pointers as Python ints)
+# ---------------------------------------------------------------------------
+
+def fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, stream):
+    return load_library().fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, stream)
+
+
+def fa_bwd_workspace_size(B, H, N, d):
+    return load_library().fa_bwd_workspace_size(B, H, N, d)
+
+
+def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, causal, ws, ws_bytes, stream):
+    return load_library().fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, causal,
+                                 ws, ws_bytes, stream)
+
+
+def fa_bwd_prep(o, dout, B, H, N, d, ws, ws_bytes, stream):
+    return load_library().fa_bwd_prep(o, dout, B, H, N, d, ws, ws_bytes, stream)
+
+
+def fa_bwd_main(q, k, v, lse, dout, dk, dv, B, H, N, d, scale, causal, ws, ws_bytes, stream):
+    return load_library().fa_bwd_main(q, k, v, lse, dout, dk, dv, B, H, N, d, scale, causal,
+                                      ws, ws_bytes, stream)
+
+
+def fa_bwd_finish(dq, B, H, N, d, ws, ws_bytes, stream):
+    return load_library().fa_bwd_finish(dq, B, H, N, d, ws, ws_bytes, stream)
+
+
+def fa_sync_status(stream):
+    return load_library().fa_sync_status(stream)
+
+
+def fa_status_string(code):
+    return load_library().fa_status_string(code)
+
+
+def fa_version():
+    return load_library().fa_version()
+
+
+def status_string(code: int) -> str:
+    try:
+        return fa_status_string(code).decode()
+    except Exception:  # library not loadable: still name the code
+        return str(code)
+
+
+def _check(rc: int, what: str):
+    if rc != FA_OK:
+        raise FAError(rc, what)
+
+
+# ---------------------------------------------------------------------------
+# torch marshalling
+# ---------------------------------------------------------------------------
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream_handle(stream=None) -> int:
+    torch = _torch()
+    s = torch.cuda.current_stream() if stream is None else stream
+    return int(s.cuda_stream)
+
+
+def _check_qkv(*ts):
+    torch = _torch()
+    ref = ts[0]
+    if ref.dim() != 4:
+        raise ValueError("tensors are [B, H, N, d]")
+    for t in ts:
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("tensors must be contiguous bf16 CUDA tensors")
+        if t.shape != ref.shape or t.device != ref.device:
+            raise ValueError("tensors must share shape and device")
+    return tuple(ref.shape)
+
+
+def forward(q, k, v, scale=None, causal=False, out=None, lse=None, stream=None):
+    """O, lse = attention(q, k, v).  q, k, v: bf16 [B, H, N, d] on the GPU.
+    Returns (o bf16 [B,H,N,d], lse fp32 [B,H,N])."""
+    torch = _torch()
+    B, H, N, d = _check_qkv(q, k, v)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    _check_qkv(q, out)
+    if lse.dtype != torch.float32 or not lse.is_contiguous() or lse.shape != (B, H, N):
+        raise ValueError("lse must be contiguous fp32 [B, H, N]")
+    rc = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                B, H, N, d, scale, int(bool(causal)), _stream_handle(stream))
+    _check(rc, "fa_fwd")
+    return out, lse
+
+
+def workspace_bytes(B, H, N, d) -> int:
+    return int(fa_bwd_workspace_size(B, H, N, d))
+
+
+def alloc_workspace(B, H, N, d, device):
+    torch = _torch()
+    return torch.empty(workspace_bytes(B, H, N, d), dtype=torch.uint8, device=device)
+
+
+def backward(q, k, v, o, lse, dout, scale=None, causal=False, dq=None, dk=None, dv=None,
+             workspace=None, stream=None):
+    """dq, dk, dv of attention given the forward's o and lse and dL/dO."""
+    torch = _torch()
+    B, H, N, d = _check_qkv(q, k, v, o, dout)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _check_qkv(q, dq, dk, dv)
+    if lse.dtype != torch.float32 or not lse.is_contiguous() or lse.shape != (B, H, N):
+        raise ValueError("lse must be contiguous fp32 [B, H, N]")
+    if workspace is None:
+        workspace = alloc_workspace(B, H, N, d, q.device)
+    rc = fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                B, H, N, d, scale, int(bool(causal)), workspace.data_ptr(), workspace.numel(),
+                _stream_handle(stream))
+    _check(rc, "fa_bwd")
+    return dq, dk, dv
+
+
+def sync_status(stream=None):
+    """Synchronise the stream and raise if a kernel reported a device timeout."""
+    _check(fa_sync_status(_stream_handle(stream)), "device status")

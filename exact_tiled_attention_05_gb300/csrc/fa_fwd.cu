@@ -1,0 +1,414 @@
+// fa_fwd.cu -- fused exact-attention forward pass for sm_103a.
+//
+// One CTA owns 256 query rows of one (batch, head): two 128-row Q tiles that
+// share every K/V tile it streams ("FlashAttention 1–4" §"FlashAttention-2":
+// a thread block per query block, K/V streamed in the inner loop; two Q tiles
+// per CTA as in §"FlashAttention-4").  Roles, by warp:
+//   warp 0      TMA producer: Q tiles once, then K_j, V_j into a ring of
+//               shared-memory stages guarded by full/empty mbarriers.
+//   warp 1      MMA issuer: S_t = Q_t K_j^T and O_t += P_t V_j on the tcgen05
+//               tensor cores, accumulators in tensor memory (TMEM).
+//   warp 2      allocates / frees TMEM.
+//   warps 4-7   softmax for Q tile 0, warps 8-11 for Q tile 1: one thread per
+//               query row reads its S row from TMEM, applies the causal/tail
+//               mask, runs the online-softmax update, writes P (bf16) back into
+//               TMEM over S, and at the end normalises O and writes O and lse.
+//
+// Online softmax ("07 GPU、资源估算与 FlashAttention" §7.8; "CS336 Lecture 5
+// notes" §11.3-§11.4): per row a running max m (log2 units of the scaled
+// score), a running sum l and the unnormalised accumulator O in TMEM.  When a
+// tile raises m, O and l are rescaled by exp2(m_old - m_new) before that tile's
+// P V is accumulated; warps whose rows all kept their max skip the O pass.
+// lse = (m + log2 l) * ln 2.
+//
+// Causal: key tiles entirely in the future of a Q tile are never loaded or
+// multiplied; the diagonal tile and a ragged last tile are masked per element.
+#include "fa_internal.cuh"
+#include "ptx.cuh"
+
+namespace fa {
+namespace {
+
+using namespace ptx;
+
+constexpr int kBM = 128;        // query rows per Q tile
+constexpr int kBN = 128;        // keys per K/V tile
+constexpr int kThreads = 384;   // 12 warps
+constexpr int kBoxBytes = 128 * 64 * 2;  // one TMA box: 128 rows x 64 bf16
+// The reference max follows the running max exactly (threshold 0).  A stale
+// reference (FA4's conditional rescaling, threshold 8) keeps O / l exact in
+// real arithmetic, but the dominant probability becomes 2^delta instead of
+// exactly 1.0 and picks up bf16 rounding in P; on rows close to one-hot that
+// alone moves O by more than 1e-2.  With an exact max the largest weight of
+// every row is exactly 1.0.
+constexpr float kRescaleThreshold = 0.0f;  // log2 units
+
+template <int HD>
+struct FwdCfg {
+    static constexpr int kTileBytes = kBN * HD * 2;
+    static constexpr int kBoxes = HD / 64;
+    static constexpr int kStages = HD == 128 ? 4 : 8;
+    static constexpr uint32_t kSColStride = 128;  // S_t at TMEM column t * 128
+    static constexpr uint32_t kOCol0 = 256;
+    static constexpr uint32_t kTmemCols = 512;
+};
+
+template <int HD>
+struct alignas(1024) FwdSmem {
+    uint8_t q[2][FwdCfg<HD>::kTileBytes];
+    uint8_t kv[FwdCfg<HD>::kStages][FwdCfg<HD>::kTileBytes];
+    uint64_t q_full;
+    uint64_t kv_full[FwdCfg<HD>::kStages];
+    uint64_t kv_empty[FwdCfg<HD>::kStages];
+    uint64_t s_full[2];
+    uint64_t p_full[2];
+    uint64_t o_done[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+};
+
+__device__ __forceinline__ void record_timeout(FwdArgs const& a, volatile int* abort) {
+    *abort = 1;
+    atomicExch(a.status, kErrDeviceTimeout);
+}
+
+template <int HD>
+__global__ void __launch_bounds__(kThreads, 1)
+fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+              const __grid_constant__ CUtensorMap tv, const FwdArgs args) {
+    using Cfg = FwdCfg<HD>;
+    extern __shared__ uint8_t smem_raw[];
+    FwdSmem<HD>& sm = *reinterpret_cast<FwdSmem<HD>*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    volatile int* abort = &sm.abort;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int N = args.N;
+    const int BH = args.BH;
+
+    // ---- work unit: (head, 256-row query block); heavy causal blocks first ----
+    int bh, qb;
+    if (args.causal) {
+        qb = args.n_qblk - 1 - static_cast<int>(blockIdx.x) / BH;
+        bh = static_cast<int>(blockIdx.x) % BH;
+    } else {
+        bh = static_cast<int>(blockIdx.x) / args.n_qblk;
+        qb = static_cast<int>(blockIdx.x) % args.n_qblk;
+    }
+    const int n_kv_all = (N + kBN - 1) / kBN;
+    int q0[2], nkv[2];
+    for (int t = 0; t < 2; ++t) {
+        q0[t] = qb * 2 * kBM + t * kBM;
+        if (q0[t] >= N) {
+            nkv[t] = 0;  // tile beyond the sequence: inactive
+        } else if (args.causal) {
+            const int last_q = min(q0[t] + kBM, N) - 1;
+            nkv[t] = last_q / kBN + 1;
+        } else {
+            nkv[t] = n_kv_all;
+        }
+    }
+    const int nmax = max(nkv[0], nkv[1]);
+
+    if (threadIdx.x == 0) {
+        sm.abort = 0;
+        mbar_init(smem_u32(&sm.q_full), 1);
+        for (int s = 0; s < Cfg::kStages; ++s) {
+            mbar_init(smem_u32(&sm.kv_full[s]), 1);
+            mbar_init(smem_u32(&sm.kv_empty[s]), 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(smem_u32(&sm.s_full[t]), 1);
+            mbar_init(smem_u32(&sm.p_full[t]), kBM);
+            mbar_init(smem_u32(&sm.o_done[t]), 1);
+        }
+        mbar_init(smem_u32(&sm.drain), 1);
+        fence_mbar_init();
+    }
+    if (warp == 2) {
+        tmem_alloc(smem_u32(&sm.tmem_base), Cfg::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = sm.tmem_base;
+
+    if (warp == 0) {
+        // ===================== TMA producer =====================
+        if (elect_one()) {
+            tma_prefetch_desc(&tq);
+            tma_prefetch_desc(&tk);
+            tma_prefetch_desc(&tv);
+            const uint32_t qbar = smem_u32(&sm.q_full);
+            const int nact = (nkv[0] > 0) + (nkv[1] > 0);
+            mbar_arrive_expect_tx(qbar, nact * Cfg::kTileBytes);
+            for (int t = 0; t < 2; ++t) {
+                if (nkv[t] == 0) continue;
+                for (int b = 0; b < Cfg::kBoxes; ++b)
+                    tma_load_3d(smem_u32(sm.q[t] + b * kBoxBytes), &tq, qbar, b * 64, q0[t], bh);
+            }
+            int issued = 0;
+            for (int idx = 0; idx < 2 * nmax; ++idx) {
+                const int slot = idx % Cfg::kStages;
+                const uint32_t ph = (idx / Cfg::kStages) & 1;
+                if (!mbar_wait(smem_u32(&sm.kv_empty[slot]), ph ^ 1, kWaitTimeoutNs, abort)) {
+                    record_timeout(args, abort);
+                    break;
+                }
+                const uint32_t fbar = smem_u32(&sm.kv_full[slot]);
+                mbar_arrive_expect_tx(fbar, Cfg::kTileBytes);
+                const CUtensorMap* map = (idx & 1) ? &tv : &tk;
+                const int row = (idx >> 1) * kBN;
+                for (int b = 0; b < Cfg::kBoxes; ++b)
+                    tma_load_3d(smem_u32(sm.kv[slot] + b * kBoxBytes), map, fbar, b * 64, row, bh);
+                ++issued;
+            }
+            // Let every copy that was issued land before the CTA can exit.
+            for (int slot = 0; slot < Cfg::kStages && slot < issued; ++slot) {
+                const int last = slot + Cfg::kStages * ((issued - 1 - slot) / Cfg::kStages);
+                mbar_wait(smem_u32(&sm.kv_full[slot]), (last / Cfg::kStages) & 1, kWaitTimeoutNs,
+                          abort);
+            }
+            mbar_wait(qbar, 0, kWaitTimeoutNs, abort);
+        }
+    } else if (warp == 1) {
+        // ===================== MMA issuer =====================
+        if (elect_one()) {
+            constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, 0, 0);
+            constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, HD, 0, 1);
+            const uint32_t q_addr[2] = {smem_u32(sm.q[0]), smem_u32(sm.q[1])};
+            bool ok = mbar_wait(smem_u32(&sm.q_full), 0, kWaitTimeoutNs, abort);
+            auto wait_kv = [&](int idx) -> bool {
+                return mbar_wait(smem_u32(&sm.kv_full[idx % Cfg::kStages]),
+                                 (idx / Cfg::kStages) & 1, kWaitTimeoutNs, abort);
+            };
+            auto kv_addr = [&](int idx) -> uint32_t { return smem_u32(sm.kv[idx % Cfg::kStages]); };
+            // S_t = Q_t K^T : K-major A and B, HD/16 k-steps of 16.
+            auto issue_s = [&](int t, uint32_t k_addr) {
+#pragma unroll
+                for (int kk = 0; kk < HD / 16; ++kk) {
+                    const uint32_t off = (kk / 4) * kBoxBytes + (kk % 4) * 32;
+                    umma_ss(tbase + (static_cast<uint32_t>(t) * Cfg::kSColStride), sdesc_sw128(q_addr[t] + off, 16, 1024),
+                            sdesc_sw128(k_addr + off, 16, 1024), idesc_s, kk > 0);
+                }
+            };
+            // O_t += P_t V : P (bf16) from TMEM, V MN-major, kBN/16 k-steps.
+            auto issue_pv = [&](int t, uint32_t v_addr, bool acc) {
+#pragma unroll
+                for (int kk = 0; kk < kBN / 16; ++kk) {
+                    umma_ts(tbase + Cfg::kOCol0 + t * HD, tbase + (static_cast<uint32_t>(t) * Cfg::kSColStride) + kk * 8,
+                            sdesc_sw128(v_addr + kk * 16 * 128, kBoxBytes, 1024), idesc_o,
+                            (acc || kk > 0) ? 1u : 0u);
+                }
+            };
+            if (ok && nmax > 0) {
+                ok = wait_kv(0);
+                if (ok) {
+                    tc_fence_after();
+                    for (int t = 0; t < 2; ++t) {
+                        if (nkv[t] == 0) continue;
+                        issue_s(t, kv_addr(0));
+                        umma_commit(smem_u32(&sm.s_full[t]));
+                    }
+                    umma_commit(smem_u32(&sm.kv_empty[0]));
+                }
+            }
+            for (int j = 0; ok && j < nmax; ++j) {
+                const int iv = 2 * j + 1, ik = 2 * j + 2;
+                if (!(ok = wait_kv(iv))) break;
+                tc_fence_after();
+                bool k_ready = false;
+                for (int t = 0; t < 2 && ok; ++t) {
+                    if (j < nkv[t]) {
+                        if (!(ok = mbar_wait(smem_u32(&sm.p_full[t]), j & 1, kWaitTimeoutNs, abort)))
+                            break;
+                        tc_fence_after();
+                        issue_pv(t, kv_addr(iv), j > 0);
+                        umma_commit(smem_u32(&sm.o_done[t]));
+                    }
+                    if (t == 1) umma_commit(smem_u32(&sm.kv_empty[iv % Cfg::kStages]));
+                    if (j + 1 < nkv[t]) {
+                        if (!k_ready) {
+                            if (!(ok = wait_kv(ik))) break;
+                            tc_fence_after();
+                            k_ready = true;
+                        }
+                        // S_t(j+1) overwrites P_t(j) only after PV_t(j) was issued;
+                        // the tensor pipe executes one thread's MMAs in order.
+                        issue_s(t, kv_addr(ik));
+                        umma_commit(smem_u32(&sm.s_full[t]));
+                    }
+                }
+                if (ok && k_ready) umma_commit(smem_u32(&sm.kv_empty[ik % Cfg::kStages]));
+            }
+            if (!ok) record_timeout(args, abort);
+            // Every MMA (and every commit before it) completes before the CTA leaves.
+            umma_commit(smem_u32(&sm.drain));
+            mbar_wait(smem_u32(&sm.drain), 0, kWaitTimeoutNs, abort);
+        }
+    } else if (warp >= 4) {
+        // ===================== softmax / epilogue =====================
+        const int t = (warp - 4) >> 2;
+        const int wq = warp & 3;  // TMEM lane quarter this warp may access
+        const int row = wq * 32 + lane;
+        const int qi = q0[t] + row;
+        const uint32_t lane_addr = tbase + (static_cast<uint32_t>(wq * 32) << 16);
+        const uint32_t s_addr = lane_addr + (static_cast<uint32_t>(t) * Cfg::kSColStride);
+        const uint32_t o_addr = lane_addr + Cfg::kOCol0 + t * HD;
+        const float sl2 = args.scale_log2;
+        float m_ref = -INFINITY;  // reference max, log2 units
+        float l_sum = 0.f;
+        bool ok = true;
+        for (int j = 0; j < nkv[t]; ++j) {
+            ok = mbar_wait(smem_u32(&sm.s_full[t]), j & 1, kWaitTimeoutNs, abort);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            tc_fence_after();
+            float s[kBN];
+            {
+                uint32_t r0[32], r1[32], r2[32], r3[32];
+                tmem_ld32(s_addr + 0, r0);
+                tmem_ld32(s_addr + 32, r1);
+                tmem_ld32(s_addr + 64, r2);
+                tmem_ld32(s_addr + 96, r3);
+                tmem_wait_ld();
+                reg_fence(r0);
+                reg_fence(r1);
+                reg_fence(r2);
+                reg_fence(r3);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    s[i] = __uint_as_float(r0[i]);
+                    s[32 + i] = __uint_as_float(r1[i]);
+                    s[64 + i] = __uint_as_float(r2[i]);
+                    s[96 + i] = __uint_as_float(r3[i]);
+                }
+            }
+            const int kbase = j * kBN;
+            const bool edge = (kbase + kBN > N) || (args.causal && kbase + kBN - 1 > q0[t]);
+            if (edge) {
+                const int kend = args.causal ? min(N, qi + 1) : N;
+#pragma unroll
+                for (int c = 0; c < kBN; ++c)
+                    if (kbase + c >= kend) s[c] = -INFINITY;
+            }
+            float mx = s[0];
+#pragma unroll
+            for (int c = 1; c < kBN; ++c) mx = fmaxf(mx, s[c]);
+            const float mx2 = mx * sl2;
+            // reference-max update (conditional rescaling)
+            bool rescale = false;
+            float alpha = 1.f;
+            if (m_ref == -INFINITY) {
+                m_ref = mx2;
+            } else if (mx2 > m_ref + kRescaleThreshold) {
+                rescale = true;
+                alpha = ex2(m_ref - mx2);
+                l_sum *= alpha;
+                m_ref = mx2;
+            }
+            if (__any_sync(0xffffffffu, rescale)) {
+                // O already holds PV of earlier tiles: wait for the latest one.
+                ok = mbar_wait(smem_u32(&sm.o_done[t]), (j - 1) & 1, kWaitTimeoutNs, abort);
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                tc_fence_after();
+                uint32_t r[32];
+#pragma unroll 1
+                for (int c = 0; c < HD / 32; ++c) {
+                    tmem_ld32(o_addr + c * 32, r);
+                    tmem_wait_ld();
+                    reg_fence(r);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                    tmem_st32(o_addr + c * 32, r);
+                }
+                tmem_wait_st();
+            }
+            const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
+            // P = exp2(s * scale * log2e - m), packed bf16 pairs over S columns [0, 64)
+#pragma unroll
+            for (int c = 0; c < kBN / 32; ++c) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float p0 = ex2(fmaf(s[c * 32 + 2 * i], sl2, neg_m));
+                    const float p1 = ex2(fmaf(s[c * 32 + 2 * i + 1], sl2, neg_m));
+                    l_sum += p0 + p1;
+                    pk[i] = pack_bf16x2(p0, p1);
+                }
+                tmem_st16(s_addr + c * 16, pk);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(smem_u32(&sm.p_full[t]));
+        }
+        if (!ok) {
+            if (lane == 0) record_timeout(args, abort);
+        } else if (nkv[t] > 0) {
+            ok = mbar_wait(smem_u32(&sm.o_done[t]), (nkv[t] - 1) & 1, kWaitTimeoutNs, abort);
+            if (__all_sync(0xffffffffu, ok)) {
+                tc_fence_after();
+                const float inv_l = 1.f / l_sum;
+                const bool store = qi < N;
+                const size_t row_off = (static_cast<size_t>(bh) * N + qi) * HD;
+                uint8_t* orow = reinterpret_cast<uint8_t*>(args.o) + row_off * 2;
+                uint32_t r[32];
+#pragma unroll 1
+                for (int c = 0; c < HD / 32; ++c) {
+                    tmem_ld32(o_addr + c * 32, r);
+                    tmem_wait_ld();
+                    reg_fence(r);
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * inv_l,
+                                            __uint_as_float(r[2 * i + 1]) * inv_l);
+                    if (store) {
+#pragma unroll
+                        for (int v4 = 0; v4 < 4; ++v4)
+                            st_global_v4(orow + c * 64 + v4 * 16, pk[4 * v4], pk[4 * v4 + 1],
+                                         pk[4 * v4 + 2], pk[4 * v4 + 3]);
+                    }
+                }
+                if (store)
+                    args.lse[static_cast<size_t>(bh) * N + qi] =
+                        (m_ref + __log2f(l_sum)) * 0.69314718055994531f;
+            } else if (lane == 0) {
+                record_timeout(args, abort);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tbase, Cfg::kTmemCols);
+    }
+}
+
+template <int HD>
+cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                         const FwdArgs& args, cudaStream_t stream) {
+    const size_t smem = sizeof(FwdSmem<HD>) + 1024;
+    cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<HD>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    const unsigned grid = static_cast<unsigned>(args.n_qblk) * static_cast<unsigned>(args.BH);
+    fa_fwd_kernel<HD><<<grid, kThreads, smem, stream>>>(tq, tk, tv, args);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const FwdArgs& args, cudaStream_t stream) {
+    if (d == 64) return launch_fwd_t<64>(tq, tk, tv, args, stream);
+    return launch_fwd_t<128>(tq, tk, tv, args, stream);
+}
+
+}  // namespace fa

@@ -1,0 +1,73 @@
+// fa_internal.cuh -- parameters and launch entry points shared between the
+// host API (fa_api.cu) and the kernel translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace fa {
+
+// Status codes (mirror fa_status in include/fa.h).
+enum : int {
+    kOk = 0,
+    kErrInvalidArg = 1,
+    kErrUnsupported = 2,
+    kErrMisaligned = 3,
+    kErrWorkspace = 4,
+    kErrCuda = 5,
+    kErrDeviceTimeout = 6,
+};
+
+// A kernel that waits longer than this on one barrier gives up.
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
+
+struct FwdArgs {
+    void* o;          // bf16 [BH, N, d]
+    float* lse;       // fp32 [BH, N]
+    int BH;
+    int N;
+    int n_qblk;       // query blocks (256 rows each) per head
+    int causal;
+    float scale_log2; // scale * log2(e)
+    int* status;      // device status word
+};
+
+struct BwdArgs {
+    const void* q;    // bf16 [BH, N, d] (plain pointers for the row-wise stages)
+    const void* k;
+    const void* v;
+    const void* o;
+    const void* dout;
+    const float* lse; // fp32 [BH, N]
+    void* dq;
+    void* dk;
+    void* dv;
+    float* dq_acc;    // fp32 [BH, N, d] workspace
+    float* delta;     // fp32 [BH, N] workspace: rowsum(dO * O)
+    int BH;
+    int N;
+    int n_kblk;       // key blocks (128 rows) per head
+    int causal;
+    float scale;
+    float scale_log2;
+    int* status;
+};
+
+// Tensor maps for one [BH, N, d] bf16 tensor: box of 64 columns x 128 rows,
+// 128-byte swizzle (what the UMMA shared-memory descriptors expect).
+struct TensorMaps3 {
+    CUtensorMap a, b, c;
+};
+
+// Launchers (defined in the kernel translation units).  Return a cudaError_t.
+cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const FwdArgs& args, cudaStream_t stream);
+cudaError_t launch_bwd_prep(int d, const BwdArgs& args, cudaStream_t stream);
+cudaError_t launch_bwd_main(int d, const CUtensorMap& tq, const CUtensorMap& tk,
+                            const CUtensorMap& tv, const CUtensorMap& tdo, const BwdArgs& args,
+                            cudaStream_t stream);
+cudaError_t launch_bwd_finish(int d, const BwdArgs& args, cudaStream_t stream);
+
+}  // namespace fa

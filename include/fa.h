@@ -1,0 +1,109 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) exact-attention library (libfa.so).
+ *
+ * The library computes exact scaled-dot-product attention
+ *
+ *     O = softmax(scale * Q K^T [+ causal mask]) V,   lse = per-row logsumexp,
+ *
+ * as one fused tiled kernel that never writes the N x N score or probability
+ * matrix to memory ("GPU 与 TPU：让硬件不再是黑魔法" (CS336 Lecture 5 notes)
+ * §11.4; "FlashAttention 1–4: How IO-Awareness Reshaped the Attention Kernel"
+ * §"FlashAttention (v1)" and §"FlashAttention-2"), and the backward pass that
+ * rebuilds the probabilities from the saved logsumexp (CS336 Lecture 5 notes
+ * §11.5 (3): P = exp(S - L)).
+ *
+ * Common conventions
+ *  - Tensors q, k, v, o, dout, dq, dk, dv: bfloat16, contiguous [B, H, N, d]
+ *    row-major (d innermost), passed as untyped device pointers, 16-byte aligned.
+ *  - lse: fp32 [B, H, N], natural logarithm of the row's sum of
+ *    exp(scale * q.k) over the visible keys (L = m + log l).
+ *  - d (head dimension) is 64 or 128; N >= 1 (any length, tails are masked);
+ *    B, H >= 1; B*H*N*d < 2^31.  scale is finite and non-zero (callers usually
+ *    pass 1/sqrt(d)); causal is 0 or 1 (key j visible to query i iff j <= i).
+ *  - Every pointer is caller-owned device memory; the library keeps no pointer
+ *    after a call returns and allocates no device memory per call.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t, 0 = legacy default
+ *    stream) and may be issued from several host threads.
+ *  - Argument errors are returned before anything is launched.  A failed launch
+ *    returns FA_ERR_CUDA.  Every wait inside the kernels is bounded: a kernel
+ *    that gives up records FA_ERR_DEVICE_TIMEOUT in a device status word that
+ *    fa_sync_status() reports.  Nothing is printed and nothing aborts.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1,   /* null pointer, bad size, non-finite scale ... */
+    FA_ERR_UNSUPPORTED = 2,   /* head dim not 64/128, or no sm_103 device     */
+    FA_ERR_MISALIGNED = 3,    /* a tensor pointer is not 16-byte aligned      */
+    FA_ERR_WORKSPACE = 4,     /* backward workspace missing or too small      */
+    FA_ERR_CUDA = 5,          /* a CUDA runtime/driver call failed            */
+    FA_ERR_DEVICE_TIMEOUT = 6 /* a kernel wait expired (see fa_sync_status)   */
+} fa_status;
+
+/* Forward pass.  Writes o (bf16 [B,H,N,d]) and lse (fp32 [B,H,N]).
+ * Steps: scores S = scale*Q K^T tile by tile on the tensor cores, online
+ * softmax with a running max m and running sum l per row, unnormalised output
+ * accumulator rescaled when the max moves, one normalisation O = acc / l at the
+ * end, lse = m + ln l ("FlashAttention 1–4" §"FlashAttention (v1)" recurrence;
+ * "07 GPU、资源估算与 FlashAttention" §7.8).  `stream` is a cudaStream_t. */
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+           int B, int H, int N, int d, float scale, int causal, void* stream);
+
+/* Bytes of device workspace fa_bwd needs for these sizes: an fp32 dQ
+ * accumulator [B,H,N,d] and the fp32 row statistic D = rowsum(dO * O) [B,H,N],
+ * each rounded up to 256 bytes. */
+size_t fa_bwd_workspace_size(int B, int H, int N, int d);
+
+/* Backward pass.  Inputs q, k, v, o, lse (as written by fa_fwd) and dout
+ * (dL/dO); outputs dq, dk, dv (bf16 [B,H,N,d]).  workspace: caller-owned
+ * device memory of at least fa_bwd_workspace_size() bytes, 256-byte aligned;
+ * its contents on entry do not matter.  Runs fa_bwd_prep, fa_bwd_main and
+ * fa_bwd_finish in order on `stream`.
+ * The pages state only that P is recomputed from Q, K and the saved L and that
+ * the gradients follow; the formulas used are the softmax Jacobian:
+ *   dV = P^T dO, dP = dO V^T, D = rowsum(dO * O), dS = P * (dP - D),
+ *   dQ = scale * dS K, dK = scale * dS^T Q. */
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+           const void* dout, void* dq, void* dk, void* dv,
+           int B, int H, int N, int d, float scale, int causal,
+           void* workspace, size_t workspace_bytes, void* stream);
+
+/* The three stages of fa_bwd, exposed so a caller can time or overlap them.
+ * prep:   D = rowsum(dO * O) into the workspace and clears the dQ accumulator.
+ * main:   per key/value tile, recompute S and P = exp(S - lse), accumulate
+ *         dV and dK on chip and add scale * dS K into the dQ accumulator.
+ * finish: dq = bf16(dQ accumulator).
+ * Arguments mean the same as for fa_bwd; each stage reads what the previous
+ * one wrote into the workspace. */
+int fa_bwd_prep(const void* o, const void* dout, int B, int H, int N, int d,
+                void* workspace, size_t workspace_bytes, void* stream);
+int fa_bwd_main(const void* q, const void* k, const void* v, const float* lse,
+                const void* dout, void* dk, void* dv,
+                int B, int H, int N, int d, float scale, int causal,
+                void* workspace, size_t workspace_bytes, void* stream);
+int fa_bwd_finish(void* dq, int B, int H, int N, int d,
+                  void* workspace, size_t workspace_bytes, void* stream);
+
+/* Synchronises `stream`, then returns and clears the device status word of the
+ * current device: FA_OK, or FA_ERR_DEVICE_TIMEOUT if any kernel gave up on a
+ * wait since the last call, or FA_ERR_CUDA if the synchronisation failed. */
+int fa_sync_status(void* stream);
+
+/* Static, human-readable name of a status code. */
+const char* fa_status_string(int status);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FA_GB300_H */

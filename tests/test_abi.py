@@ -1,0 +1,112 @@
+"""The C ABI without a GPU: the library loads, exports every function that
+include/fa.h declares, and rejects bad arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import exact_tiled_attention_05_gb300 as fa
+from exact_tiled_attention_05_gb300 import build as fa_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fa_build.build()
+    return fa.load_library()
+
+
+def declared_functions():
+    names = []
+    for hdr in os.listdir(os.path.join(ROOT, "include")):
+        if not hdr.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", hdr)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"\b(fa_\w+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_every_declared_function_is_exported(lib):
+    names = declared_functions()
+    assert "fa_fwd" in names and "fa_bwd" in names
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+        assert n in fa.EXPORTED
+
+
+def test_status_strings(lib):
+    for code, name in ((0, "FA_OK"), (1, "FA_ERR_INVALID_ARG"), (6, "FA_ERR_DEVICE_TIMEOUT")):
+        assert fa.fa_status_string(code).decode() == name
+    assert fa.fa_status_string(99).decode() == "FA_ERR_UNKNOWN"
+    assert fa.fa_version() >= 100
+
+
+def test_workspace_size(lib):
+    B, H, N, d = 2, 3, 100, 64
+    rows = B * H * N
+    r256 = lambda x: (x + 255) // 256 * 256
+    assert fa.fa_bwd_workspace_size(B, H, N, d) == r256(rows * d * 4) + r256(rows * 4)
+    assert fa.fa_bwd_workspace_size(0, 1, 1, 64) == 0
+
+
+FAKE = 0x100000  # 16-byte aligned, never dereferenced: validation fails first
+
+
+def test_fwd_argument_errors(lib):
+    args = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=1, H=1, N=128, d=64,
+                scale=0.125, causal=0, stream=None)
+
+    def call(**kw):
+        a = dict(args, **kw)
+        return fa.fa_fwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["N"],
+                         a["d"], a["scale"], a["causal"], a["stream"])
+
+    assert call(q=None) == fa.FA_ERR_INVALID_ARG
+    assert call(lse=None) == fa.FA_ERR_INVALID_ARG
+    assert call(N=0) == fa.FA_ERR_INVALID_ARG
+    assert call(B=-1) == fa.FA_ERR_INVALID_ARG
+    assert call(causal=2) == fa.FA_ERR_INVALID_ARG
+    assert call(scale=float("nan")) == fa.FA_ERR_INVALID_ARG
+    assert call(scale=float("inf")) == fa.FA_ERR_INVALID_ARG
+    assert call(scale=0.0) == fa.FA_ERR_INVALID_ARG
+    assert call(d=96) == fa.FA_ERR_UNSUPPORTED
+    assert call(d=256) == fa.FA_ERR_UNSUPPORTED
+    assert call(B=1 << 12, H=1 << 12, N=1 << 8) == fa.FA_ERR_INVALID_ARG  # >= 2^31 elements
+    assert call(q=FAKE + 8) == fa.FA_ERR_MISALIGNED
+    assert call(o=FAKE + 2) == fa.FA_ERR_MISALIGNED
+    assert call(lse=FAKE + 2) == fa.FA_ERR_MISALIGNED
+
+
+def test_bwd_argument_errors(lib):
+    ws = fa.fa_bwd_workspace_size(1, 1, 128, 64)
+    base = [FAKE] * 9 + [1, 1, 128, 64, 0.125, 1, FAKE, ws, None]
+
+    def call(i=None, val=None):
+        a = list(base)
+        if i is not None:
+            a[i] = val
+        return fa.fa_bwd(*a)
+
+    assert call(0, None) == fa.FA_ERR_INVALID_ARG
+    assert call(8, None) == fa.FA_ERR_INVALID_ARG
+    assert call(12, 80) == fa.FA_ERR_UNSUPPORTED
+    assert call(15, None) == fa.FA_ERR_WORKSPACE
+    assert call(15, FAKE + 16) == fa.FA_ERR_WORKSPACE  # not 256-byte aligned
+    assert call(16, ws - 1) == fa.FA_ERR_WORKSPACE
+    assert fa.fa_bwd_prep(None, FAKE, 1, 1, 128, 64, FAKE, ws, None) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_bwd_finish(None, 1, 1, 128, 64, FAKE, ws, None) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_bwd_main(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 128, 64, 0.125, 1,
+                          FAKE, 16, None) == fa.FA_ERR_WORKSPACE
+
+
+def test_library_is_the_in_tree_build(lib):
+    assert os.path.dirname(fa.LIB_PATH) == os.path.join(ROOT, "exact_tiled_attention_05_gb300")
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    monkeypatch.setattr(fa, "_lib", None)
+    with pytest.raises(RuntimeError):
+        fa.load_library(str(tmp_path / "nope.so"))

@@ -1,0 +1,230 @@
+"""Forward pass on the GPU, through the C ABI, against the fp64 oracle."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import exact_tiled_attention_05_gb300 as fa
+from exact_tiled_attention_05_gb300 import workloads as wl
+from parity import (bf16_half_ulp, bits, check_lse, check_o, check_o_beyond_rounding, o_report,
+                    to_np, with_guard)
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+_cache = {}
+
+
+def run_fwd(inp, causal, scale=None):
+    q, k, v = (inp[n].to(DEV) for n in ("q", "k", "v"))
+    o, lse = fa.forward(q, k, v, scale=scale, causal=causal)
+    fa.sync_status()
+    return o, lse
+
+
+def workload_run(name, causal):
+    key = (name, causal)
+    if key not in _cache:
+        w = wl.WORKLOADS[name]
+        inp = wl.make_inputs(w)
+        o, lse = run_fwd(inp, causal, w.scale)
+        _cache[key] = (w, inp, o.cpu(), lse.cpu())
+    return _cache[key]
+
+
+# ---------------------------------------------------------------------------
+# the worked example from the pages, through the kernel
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_worked_example_three_scores(d):
+    """scores [0, ln2, ln3], V = [1, 2, 4]: O = 17/6 and lse = ln 6 for every row
+    ("07 GPU、资源估算与 FlashAttention" §7.8)."""
+    inp = wl.worked_example_inputs(d=d)
+    o, lse = run_fwd(inp, causal=False, scale=1.0)
+    o = to_np(o)[0, 0]
+    lse = to_np(lse)[0, 0]
+    assert np.all(np.abs(o[:, 0] - 17.0 / 6.0) <= 1e-2)
+    assert np.all(o[:, 1:] == 0.0)
+    assert np.all(np.abs(lse - math.log(6.0)) <= 1e-3)
+    # and the oracle on the very same bf16 inputs agrees
+    o_ref, l_ref = oracle.fwd(bits(inp["q"]), bits(inp["k"]), bits(inp["v"]), 1.0, False)
+    check_o(o, o_ref[0], "worked example")
+    check_lse(lse, l_ref[0], "worked example")
+
+
+# ---------------------------------------------------------------------------
+# the workloads, element by element
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_single_head_256(causal):
+    w, inp, o, lse = workload_run("single_head_256", causal)
+    o_ref, l_ref = oracle.fwd(bits(inp["q"]), bits(inp["k"]), bits(inp["v"]), w.scale, causal)
+    check_o(to_np(o).reshape(o_ref.shape), o_ref, "single head 256")
+    check_lse(to_np(lse).reshape(l_ref.shape), l_ref, "single head 256")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_fwd_2k_d64_all_heads(causal):
+    w, inp, o, lse = workload_run("fwd_2k_d64", causal)
+    o_ref, l_ref = oracle.fwd(bits(inp["q"]), bits(inp["k"]), bits(inp["v"]), w.scale, causal)
+    check_o(to_np(o).reshape(o_ref.shape), o_ref, "fwd 2k d64")
+    check_lse(to_np(lse).reshape(l_ref.shape), l_ref, "fwd 2k d64")
+
+
+def test_fwd_8k_d128_kx3_sampled_rows_and_full_heads():
+    w, inp, o, lse = workload_run("fwd_8k_d128_kx3", True)
+    qb, kb, vb = bits(inp["q"]), bits(inp["k"]), bits(inp["v"])
+    o = to_np(o).reshape(w.BH, w.N, w.d)
+    lse = to_np(lse).reshape(w.BH, w.N)
+    rows = wl.sampled_rows(w, count=256)
+    o_ref, l_ref = oracle.fwd_rows(qb, kb, vb, w.scale, True, rows)
+    o_s = np.take_along_axis(o, rows[:, :, None], axis=1)
+    l_s = np.take_along_axis(lse, rows, axis=1)
+    check_o(o_s, o_ref, "8k kx3 sampled rows")
+    check_lse(l_s, l_ref, "8k kx3 sampled rows")
+    heads = [0, w.BH - 1]
+    o_h, l_h = oracle.fwd(qb, kb, vb, w.scale, True, heads=heads)
+    check_o(o[heads], o_h, "8k kx3 full heads")
+    check_lse(lse[heads], l_h, "8k kx3 full heads")
+    print("8k kx3 full heads:", o_report(o[heads], o_h))
+
+
+def test_fwd_32k_d128_sampled_rows():
+    """Long context: 512 seeded rows per head (rows 0 and N-1 always)."""
+    w = wl.WORKLOADS["fwd_32k_d128"]
+    inp = wl.make_inputs(w)
+    o, lse = run_fwd(inp, True, w.scale)
+    o = to_np(o).reshape(w.BH, w.N, w.d)
+    lse = to_np(lse).reshape(w.BH, w.N)
+    rows = wl.sampled_rows(w)
+    assert rows.shape == (w.BH, 512)
+    o_ref, l_ref = oracle.fwd_rows(bits(inp["q"]), bits(inp["k"]), bits(inp["v"]), w.scale,
+                                   True, rows)
+    check_o(np.take_along_axis(o, rows[:, :, None], axis=1), o_ref, "32k sampled rows")
+    check_lse(np.take_along_axis(lse, rows, axis=1), l_ref, "32k sampled rows")
+    # causal row 0 is exactly V[0]
+    v0 = inp["v"][0, :, 0, :].double().numpy()
+    assert np.array_equal(o[:, 0, :], v0)
+
+
+# ---------------------------------------------------------------------------
+# ragged and degenerate shapes
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("N", [1, 2, 3, 64, 127, 128, 129, 255, 256, 257, 300, 640, 1000])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_ragged_lengths(N, d, causal):
+    w = wl.WORKLOADS["single_head_256"]
+    inp = wl.make_inputs(w, B=2, H=3, N=N, d=d, seed=1000 + N + d)
+    o, lse = run_fwd(inp, causal, 1.0 / math.sqrt(d))
+    o_ref, l_ref = oracle.fwd(bits(inp["q"]), bits(inp["k"]), bits(inp["v"]), 1.0 / math.sqrt(d),
+                              causal)
+    check_o_beyond_rounding(to_np(o).reshape(o_ref.shape), o_ref, f"N={N} d={d}")
+    check_lse(to_np(lse).reshape(l_ref.shape), l_ref, f"N={N} d={d}")
+
+
+def test_many_heads_short_rows():
+    w = wl.WORKLOADS["single_head_256"]
+    inp = wl.make_inputs(w, B=16, H=40, N=96, d=128, seed=5)
+    for causal in (False, True):
+        o, lse = run_fwd(inp, causal, 0.1)
+        o_ref, l_ref = oracle.fwd(bits(inp["q"]), bits(inp["k"]), bits(inp["v"]), 0.1, causal)
+        check_o_beyond_rounding(to_np(o).reshape(o_ref.shape), o_ref, "many heads")
+        check_lse(to_np(lse).reshape(l_ref.shape), l_ref, "many heads")
+
+
+def test_large_scores_dynamic_range():
+    """Scores of magnitude ~100: the running max moves by far more than the
+    rescale threshold, many times per row."""
+    g = torch.Generator().manual_seed(3)
+    B, H, N, d = 1, 4, 1024, 128
+    q = (torch.randn(B, H, N, d, generator=g) * 4).to(torch.bfloat16)
+    k = (torch.randn(B, H, N, d, generator=g) * 4).to(torch.bfloat16)
+    # keys get larger along the sequence so the max keeps rising
+    ramp = torch.linspace(0.2, 3.0, N).view(1, 1, N, 1)
+    k = (k.float() * ramp).to(torch.bfloat16)
+    v = torch.randn(B, H, N, d, generator=g).to(torch.bfloat16)
+    inp = {"q": q, "k": k, "v": v}
+    for causal in (False, True):
+        o, lse = run_fwd(inp, causal, 1.0 / math.sqrt(d))
+        o_ref, l_ref = oracle.fwd(bits(q), bits(k), bits(v), 1.0 / math.sqrt(d), causal)
+        check_o_beyond_rounding(to_np(o).reshape(o_ref.shape), o_ref, "dynamic range")
+        check_lse(to_np(lse).reshape(l_ref.shape), l_ref, "dynamic range")
+
+
+# ---------------------------------------------------------------------------
+# invariants at full size
+# ---------------------------------------------------------------------------
+
+def test_causal_row0_equals_v0_full_size():
+    w, inp, o, lse = workload_run("fwd_8k_d128_kx3", True)
+    assert torch.equal(o[:, :, 0, :], inp["v"][:, :, 0, :])
+
+
+def test_constant_values_give_constant_output():
+    w = wl.WORKLOADS["fwd_2k_d64"]
+    inp = wl.make_inputs(w)
+    c = torch.randn(w.B, w.H, 1, w.d, generator=torch.Generator().manual_seed(9)).to(torch.bfloat16)
+    inp["v"] = c.expand(w.B, w.H, w.N, w.d).contiguous()
+    for causal in (False, True):
+        o, _ = run_fwd(inp, causal, w.scale)
+        # the weights sum to one up to fp32/bf16 rounding: O is V within one bf16 ulp
+        err = (o.cpu().double() - inp["v"].double()).abs()
+        ulp = 2.0 * torch.from_numpy(bf16_half_ulp(inp["v"].double().numpy()))
+        assert bool((err <= ulp).all()), f"max err {err.max().item()}"
+
+
+def test_key_value_permutation_invariance():
+    w = wl.WORKLOADS["fwd_2k_d64"]
+    inp = wl.make_inputs(w, B=1, H=4)
+    perm = torch.randperm(w.N, generator=torch.Generator().manual_seed(4))
+    o1, l1 = run_fwd(inp, False, w.scale)
+    inp2 = dict(inp, k=inp["k"][:, :, perm].contiguous(), v=inp["v"][:, :, perm].contiguous())
+    o2, l2 = run_fwd(inp2, False, w.scale)
+    assert (o1.float() - o2.float()).abs().max().item() <= 1e-2
+    assert (l1 - l2).abs().max().item() <= 1e-3
+
+
+# ---------------------------------------------------------------------------
+# API behaviour on the device
+# ---------------------------------------------------------------------------
+
+def test_guard_bands_untouched():
+    B, H, N, d = 2, 2, 300, 128
+    inp = wl.make_inputs(wl.WORKLOADS["single_head_256"], B=B, H=H, N=N, d=d, seed=8)
+    q, k, v = (inp[n].to(DEV) for n in ("q", "k", "v"))
+    o, chk_o = with_guard((B, H, N, d), torch.bfloat16, DEV)
+    lse, chk_l = with_guard((B, H, N), torch.float32, DEV)
+    for causal in (False, True):
+        fa.forward(q, k, v, causal=causal, out=o, lse=lse)
+        fa.sync_status()
+        chk_o()
+        chk_l()
+
+
+def test_non_default_stream_and_repeat_determinism():
+    w = wl.WORKLOADS["fwd_2k_d64"]
+    inp = wl.make_inputs(w, B=1, H=8)
+    q, k, v = (inp[n].to(DEV) for n in ("q", "k", "v"))
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        o1, l1 = fa.forward(q, k, v, causal=True)
+        o2, l2 = fa.forward(q, k, v, causal=True)
+    fa.sync_status(s)
+    s.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_device_argument_errors():
+    q = torch.zeros(1, 1, 128, 64, dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty(1, 1, 128, dtype=torch.float32, device=DEV)
+    h = torch.cuda.current_stream().cuda_stream
+    rc = fa.fa_fwd(q.data_ptr() + 2, q.data_ptr(), q.data_ptr(), q.data_ptr(), lse.data_ptr(),
+                   1, 1, 128, 64, 0.125, 0, h)
+    assert rc == fa.FA_ERR_MISALIGNED
+    assert fa.fa_sync_status(h) == fa.FA_OK

@@ -68,6 +68,9 @@ struct alignas(1024) FwdSmem {
     int abort;
 };
 
+static_assert(sizeof(FwdSmem<128>) + 1024 <= 232448, "forward d=128 shared memory exceeds 227 KB");
+static_assert(sizeof(FwdSmem<64>) + 1024 <= 232448, "forward d=64 shared memory exceeds 227 KB");
+
 __device__ __forceinline__ void record_timeout(FwdArgs const& a, volatile int* abort) {
     *abort = 1;
     atomicExch(a.status, kErrDeviceTimeout);

@@ -1,0 +1,133 @@
+"""Backward pass on the GPU, through the C ABI, against the fp64 oracle.
+
+The GPU backward consumes the GPU forward's own bf16 O and fp32 lse; the oracle
+uses its own fp64 forward.  Gradients are compared per tensor with
+max|err| / max|ref| <= 2e-2."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import exact_tiled_attention_05_gb300 as fa
+from exact_tiled_attention_05_gb300 import workloads as wl
+from parity import bits, check_grad, grad_rel, to_np, with_guard
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+def gpu_fwd_bwd(inp, causal, scale):
+    q, k, v, do = (inp[n].to(DEV) for n in ("q", "k", "v", "do"))
+    o, lse = fa.forward(q, k, v, scale=scale, causal=causal)
+    dq, dk, dv = fa.backward(q, k, v, o, lse, do, scale=scale, causal=causal)
+    fa.sync_status()
+    return o, lse, dq, dk, dv
+
+
+def small_inputs(B, H, N, d, seed):
+    w = wl.WORKLOADS["fwdbwd_4k_d128"]
+    return wl.make_inputs(w, B=B, H=H, N=N, d=d, seed=seed)
+
+
+@pytest.mark.parametrize("N", [1, 3, 64, 128, 200, 256, 384, 513])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_small_full_compare(N, d, causal):
+    B, H = 1, 3
+    scale = 1.0 / math.sqrt(d)
+    inp = small_inputs(B, H, N, d, seed=2000 + N + d + causal)
+    _, _, dq, dk, dv = gpu_fwd_bwd(inp, causal, scale)
+    g = oracle.bwd(bits(inp["q"]), bits(inp["k"]), bits(inp["v"]), bits(inp["do"]), scale, causal)
+    for got, ref, name in ((dq, g[0], "dq"), (dk, g[1], "dk"), (dv, g[2], "dv")):
+        check_grad(to_np(got).reshape(ref.shape), ref, f"{name} N={N} d={d} causal={causal}")
+
+
+def test_fwdbwd_4k_d128_sampled_heads_and_invariants():
+    """The fwd+bwd workload at full size: four heads compared in full with the
+    oracle; every head checked against sum_j dK_j = 0 and sum_j dV_j = sum_i dO_i."""
+    w = wl.WORKLOADS["fwdbwd_4k_d128"]
+    inp = wl.make_inputs(w)
+    o, lse, dq, dk, dv = gpu_fwd_bwd(inp, True, w.scale)
+    heads = [0, 21, 42, w.BH - 1]
+    g = oracle.bwd(bits(inp["q"]), bits(inp["k"]), bits(inp["v"]), bits(inp["do"]), w.scale, True,
+                   heads=heads)
+    dq_n = to_np(dq).reshape(w.BH, w.N, w.d)
+    dk_n = to_np(dk).reshape(w.BH, w.N, w.d)
+    dv_n = to_np(dv).reshape(w.BH, w.N, w.d)
+    rels = {}
+    for got, ref, name in ((dq_n, g[0], "dq"), (dk_n, g[1], "dk"), (dv_n, g[2], "dv")):
+        rels[name] = check_grad(got[heads], ref, f"{name} sampled heads")
+    print("fwdbwd 4k relative errors:", rels)
+    # the forward output of this workload also meets the forward gates
+    o_n = to_np(o).reshape(w.BH, w.N, w.d)
+    err = np.abs(o_n[heads] - g[3])
+    assert err.max() <= 1e-2 and err.mean() <= 1e-3
+    assert np.abs(to_np(lse).reshape(w.BH, w.N)[heads] - g[4]).max() <= 1e-3
+    # invariants on every head
+    sk = np.abs(dk_n.sum(axis=1)) / np.maximum(np.abs(dk_n).sum(axis=1), 1e-30)
+    assert sk.max() <= 1e-2, f"sum_j dK_j not ~0: {sk.max()}"
+    do_n = inp["do"].double().numpy().reshape(w.BH, w.N, w.d)
+    sv = np.abs(dv_n.sum(axis=1) - do_n.sum(axis=1)) / np.maximum(np.abs(dv_n).sum(axis=1), 1e-30)
+    assert sv.max() <= 1e-2, f"sum_j dV_j != sum_i dO_i: {sv.max()}"
+
+
+def test_stage_entry_points_match_fa_bwd():
+    B, H, N, d = 2, 2, 640, 128
+    scale = 1.0 / math.sqrt(d)
+    inp = small_inputs(B, H, N, d, seed=7)
+    q, k, v, do = (inp[n].to(DEV) for n in ("q", "k", "v", "do"))
+    o, lse = fa.forward(q, k, v, causal=True)
+    dq1, dk1, dv1 = fa.backward(q, k, v, o, lse, do, causal=True)
+    ws = fa.alloc_workspace(B, H, N, d, DEV)
+    dq2, dk2, dv2 = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    h = torch.cuda.current_stream().cuda_stream
+    assert fa.fa_bwd_prep(o.data_ptr(), do.data_ptr(), B, H, N, d, ws.data_ptr(), ws.numel(), h) == 0
+    assert fa.fa_bwd_main(q.data_ptr(), k.data_ptr(), v.data_ptr(), lse.data_ptr(), do.data_ptr(),
+                          dk2.data_ptr(), dv2.data_ptr(), B, H, N, d, scale, 1, ws.data_ptr(),
+                          ws.numel(), h) == 0
+    assert fa.fa_bwd_finish(dq2.data_ptr(), B, H, N, d, ws.data_ptr(), ws.numel(), h) == 0
+    fa.sync_status()
+    # dK and dV are accumulated on chip in a fixed order: bitwise equal
+    assert torch.equal(dk1, dk2) and torch.equal(dv1, dv2)
+    # dQ uses atomic adds (any order is correct): equal within tolerance
+    assert grad_rel(to_np(dq2), to_np(dq1)) <= 1e-2
+
+
+def test_guard_bands_and_workspace_reuse():
+    B, H, N, d = 1, 3, 300, 64
+    inp = small_inputs(B, H, N, d, seed=9)
+    q, k, v, do = (inp[n].to(DEV) for n in ("q", "k", "v", "do"))
+    o, lse = fa.forward(q, k, v, causal=False)
+    bufs = [with_guard((B, H, N, d), torch.bfloat16, DEV) for _ in range(3)]
+    ws = fa.alloc_workspace(B, H, N, d, DEV)
+    ws.fill_(0x7F)  # garbage in the workspace must not matter
+    outs = []
+    for _ in range(2):
+        dq, dk, dv = fa.backward(q, k, v, o, lse, do, causal=False, dq=bufs[0][0], dk=bufs[1][0],
+                                 dv=bufs[2][0], workspace=ws)
+        fa.sync_status()
+        outs.append((dq.clone(), dk.clone(), dv.clone()))
+        for _, chk in bufs:
+            chk()
+    assert torch.equal(outs[0][1], outs[1][1]) and torch.equal(outs[0][2], outs[1][2])
+    g = oracle.bwd(bits(inp["q"]), bits(inp["k"]), bits(inp["v"]), bits(inp["do"]),
+                   1.0 / math.sqrt(d), False)
+    for got, ref in zip(outs[1], g[:3]):
+        check_grad(to_np(got).reshape(ref.shape), ref, "guarded")
+
+
+def test_fwd_2k_d64_backward_both_modes():
+    """d = 64 at the size of the d = 64 forward workload (dO drawn with the same recipe)."""
+    w = wl.WORKLOADS["fwd_2k_d64"]
+    inp = wl.make_inputs(w)
+    inp["do"] = wl.random_bf16(w.shape(), seed=w.seed + 100)
+    for causal in (False, True):
+        o, lse, dq, dk, dv = gpu_fwd_bwd(inp, causal, w.scale)
+        heads = [0, w.BH - 1]
+        g = oracle.bwd(bits(inp["q"]), bits(inp["k"]), bits(inp["v"]), bits(inp["do"]), w.scale,
+                       causal, heads=heads)
+        for got, ref, name in ((dq, g[0], "dq"), (dk, g[1], "dk"), (dv, g[2], "dv")):
+            check_grad(to_np(got).reshape(w.BH, w.N, w.d)[heads], ref, f"{name} 2k d64 causal={causal}")

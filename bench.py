@@ -1,0 +1,450 @@
+"""Benchmark: exact attention fwd+bwd on GB300, TFLOP/s and % of dense BF16 peak.
+
+One step = the whole path on one batch: fa_fwd (O, lse) then fa_bwd (prep,
+main, finish -> dQ, dK, dV) on the workload B=4 H=16 N=4096 d=128, causal,
+bf16 inputs resident in HBM.  FLOPs per step follow the convention
+4*B*H*N^2*d for the forward, halved for causal, and 2.5x that for the
+backward.  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+--impl reference times the fp64 CPU oracle (the only reference this project
+has) on the host cores, on a bounded sample of the same workload per step.
+Multi-GPU runs (torchrun, one rank per GPU) are independent replicas: every
+rank runs the full workload, no data-path collective; value = all ranks' FLOPs
+divided by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import shutil
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd/bwd TFLOP/s at 1 GB300 (bf16) and % of dense BF16 tensor peak"
+WORKLOAD = "fwdbwd_4k_d128"
+FWD_GATE_WORKLOAD = "fwd_8k_d128_kx3"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def fwd_flops(w, causal=True):
+    return 4.0 * w.B * w.H * w.N * w.N * w.d / (2.0 if causal else 1.0)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas)
+# ---------------------------------------------------------------------------
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl != "reference" else "gloo"
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world, device=None):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        exe = shutil.which("nvidia-smi")
+        if not exe:
+            return
+        import tempfile
+        fd, self.path = tempfile.mkstemp(prefix="fa_clocks_", suffix=".csv")
+        os.close(fd)
+        self.out = open(self.path, "w")
+        self.proc = subprocess.Popen(
+            [exe, "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+             "-lms", "100"], stdout=self.out, stderr=subprocess.DEVNULL)
+        time.sleep(0.3)
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = sorted(r[0] for r in rows)
+        reasons = sorted({name for r in rows for name, v in zip(self.REASONS, r[3]) if v == "Active"})
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(r[2] for r in rows)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle baseline
+# ---------------------------------------------------------------------------
+
+def oracle_baseline(w, inputs_cpu, target_s=12.0, max_heads=64):
+    """fp64 oracle fwd+bwd on whole heads of the workload, all host cores,
+    adding heads until about `target_s` seconds of CPU work."""
+    import oracle
+    from exact_tiled_attention_05_gb300 import workloads as wl
+    bits = {n: wl.bf16_bits(t) for n, t in inputs_cpu.items()}
+    threads = oracle.default_threads()
+    per_head = fwd_flops(w) / w.BH * 3.5  # fwd + 2.5x bwd
+    done, spent = 0, 0.0
+    while done < max_heads and spent < target_s:
+        t0 = time.perf_counter()
+        oracle.bwd(bits["q"], bits["k"], bits["v"], bits["do"], w.scale, True, heads=[done],
+                   nthreads=threads)
+        spent += time.perf_counter() - t0
+        done += 1
+    return {"value": per_head * done / spent / 1e12, "unit": "TFLOP/s", "cores": threads,
+            "kind": "oracle",
+            "sample": f"fp64 oracle fwd+bwd of {done} of {w.BH} heads (N={w.N}, d={w.d}, causal), "
+                      f"{spent:.1f} s on {threads} host threads"}
+
+
+def run_reference(args, world, rank):
+    """--impl reference: the oracle on the host cores, same metric and config."""
+    from exact_tiled_attention_05_gb300 import workloads as wl
+    import oracle
+    w = wl.WORKLOADS[WORKLOAD]
+    if rank != 0:
+        return
+    threads = oracle.default_threads()
+    # Each step: fwd+bwd of the causal prefix of n positions of one head, with n
+    # chosen so the whole run stays within about two minutes.
+    full = wl.make_inputs(w, B=1, H=1)
+    bits = {nm: wl.bf16_bits(t) for nm, t in full.items()}
+    budget = 120.0 / max(1, args.steps + args.warmup)
+
+    def run_prefix(n):
+        sl = {nm: b[:, :n].copy() for nm, b in bits.items()}
+        t0 = time.perf_counter()
+        oracle.bwd(sl["q"], sl["k"], sl["v"], sl["do"], w.scale, True, nthreads=threads)
+        return time.perf_counter() - t0
+
+    n = 128
+    t = run_prefix(n)
+    while n < w.N and t * 4 < budget:
+        n *= 2
+        t = run_prefix(n)
+    n = min(n, w.N)
+    flops = 4.0 * n * n * w.d / 2.0 * 3.5
+    for _ in range(args.warmup):
+        run_prefix(n)
+    times = [run_prefix(n) for _ in range(args.steps)]
+    total = sum(times)
+    value = flops * args.steps / total / 1e12
+    sample = (f"fp64 oracle fwd+bwd of the first {n} positions (causal) of one head of "
+              f"B={w.B} H={w.H} N={w.N} d={w.d} per step, {threads} host threads")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(w):
+    return {"workload": f"attention fwd+bwd B={w.B} H={w.H} N={w.N} d={w.d} causal",
+            "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": True, "scale": "1/sqrt(d)",
+            "inputs": "bf16 iid N(0,1) Q, K, V, dO from a seeded CPU generator",
+            "l2": "no flush: Q, K, V, dO alone are 268 MB, larger than the 129 MB L2",
+            "parallelism": "replicas"}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def run_gpu(args, world, rank, local):
+    import torch
+    import exact_tiled_attention_05_gb300 as fa
+    from exact_tiled_attention_05_gb300 import workloads as wl
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    fa.load_library()
+    w = wl.WORKLOADS[WORKLOAD]
+    B, H, N, d = w.B, w.H, w.N, w.d
+    peaks, peak_src = load_peaks()
+
+    cpu_in = wl.make_inputs(w)  # q, k, v, do (bf16, CPU)
+    q, k, v, do = (cpu_in[n].to(dev) for n in ("q", "k", "v", "do"))
+    o = torch.empty_like(q)
+    lse = torch.empty(B, H, N, dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = fa.alloc_workspace(B, H, N, d, dev)
+    stream = torch.cuda.current_stream(dev)
+    h = stream.cuda_stream
+    scale = w.scale
+    P = lambda t: t.data_ptr()
+
+    def check(rc, what):
+        if rc != 0:
+            raise RuntimeError(f"{what}: {fa.status_string(rc)}")
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        check(fa.fa_fwd(P(q), P(k), P(v), P(o), P(lse), B, H, N, d, scale, 1, h), "fa_fwd")
+        if ev:
+            ev[1].record(stream)
+        check(fa.fa_bwd_prep(P(o), P(do), B, H, N, d, P(ws), ws.numel(), h), "fa_bwd_prep")
+        if ev:
+            ev[2].record(stream)
+        check(fa.fa_bwd_main(P(q), P(k), P(v), P(lse), P(do), P(dk), P(dv), B, H, N, d, scale, 1,
+                             P(ws), ws.numel(), h), "fa_bwd_main")
+        if ev:
+            ev[3].record(stream)
+        check(fa.fa_bwd_finish(P(dq), B, H, N, d, P(ws), ws.numel(), h), "fa_bwd_finish")
+        if ev:
+            ev[4].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    check(fa.fa_sync_status(h), "warm-up")
+
+    # ---------------- timed region: K steps on resident inputs ----------------
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clk = clocks.stop()
+    check(fa.fa_sync_status(h), "timed region")
+    elapsed_ms = t_start.elapsed_time(t_end)
+    elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
+    per = {name: sum(e[a].elapsed_time(e[b]) for e in evs) / args.steps
+           for name, a, b in (("fwd", 0, 1), ("bwd_prep", 1, 2), ("bwd_main", 2, 3),
+                              ("bwd_finish", 3, 4))}
+    f_fwd = fwd_flops(w)
+    f_step = 3.5 * f_fwd
+    value = f_step * args.steps * world / (elapsed_ms / 1e3) / 1e12
+    ms_step = elapsed_ms / args.steps
+
+    # dominant kernel: the backward main kernel
+    dom = max(per, key=per.get)
+    dom_flops = {"fwd": f_fwd, "bwd_main": 2.5 * f_fwd}.get(dom)
+    achieved = dom_flops / (per[dom] / 1e3) / 1e12 if dom_flops else None
+    peak_sus = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    peak_burst = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    roofline = {
+        "kernel": {"bwd_main": "fa_bwd_main_kernel<128>", "fwd": "fa_fwd_kernel<128>"}.get(dom, dom),
+        "bound": "tensor", "achieved": achieved, "peak": peak_sus, "unit": "TFLOP/s",
+        "frac": achieved / peak_sus if achieved else None,
+        "peak_kind": f"bf16_tflops_sustained ({peak_src}), the kernel runs inside a long step loop",
+        "frac_of_burst_peak": achieved / peak_burst if achieved else None,
+        "traffic": None,
+        "traffic_note": "ncu dram bytes per launch are summarised under profiles/",
+        "flops_per_launch": dom_flops,
+        "ms_per_launch": per[dom],
+    }
+
+    # ---------------- end to end through the public API, host buffers ----------------
+    pin = {n: t.pin_memory() for n, t in cpu_in.items()}
+    out_host = {n: torch.empty(t.shape, dtype=t.dtype).pin_memory() for n, t in
+                (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
+    h2d = sum(t.numel() * t.element_size() for t in pin.values())
+    d2h = sum(t.numel() * t.element_size() for t in out_host.values())
+    e2e_steps = max(1, min(args.steps, 50))
+
+    def e2e_step():
+        q.copy_(pin["q"], non_blocking=True)
+        k.copy_(pin["k"], non_blocking=True)
+        v.copy_(pin["v"], non_blocking=True)
+        do.copy_(pin["do"], non_blocking=True)
+        fa.forward(q, k, v, scale=scale, causal=True, out=o, lse=lse)
+        fa.backward(q, k, v, o, lse, do, scale=scale, causal=True, dq=dq, dk=dk, dv=dv,
+                    workspace=ws)
+        for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
+            out_host[n].copy_(t, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    check(fa.fa_sync_status(h), "e2e")
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    e2e = {"value": f_step * e2e_steps * world / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+           "ms_per_step": e2e_ms / e2e_steps}
+
+    # ---------------- forward gate: N = 8192, d = 128, causal ----------------
+    wg = wl.WORKLOADS[FWD_GATE_WORKLOAD]
+    gin = wl.make_inputs(wg, device=dev)
+    go = torch.empty_like(gin["q"])
+    gl = torch.empty(wg.B, wg.H, wg.N, dtype=torch.float32, device=dev)
+    for _ in range(3):
+        fa.forward(gin["q"], gin["k"], gin["v"], causal=True, out=go, lse=gl)
+    reps = 50
+    fe = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    torch.cuda.synchronize(dev)
+    for a_, b_ in fe:
+        a_.record(stream)
+        fa.forward(gin["q"], gin["k"], gin["v"], causal=True, out=go, lse=gl)
+        b_.record(stream)
+    torch.cuda.synchronize(dev)
+    check(fa.fa_sync_status(h), "forward gate")
+    fms = sorted(a_.elapsed_time(b_) for a_, b_ in fe)
+    f_gate = fwd_flops(wg) / (fms[reps // 2] / 1e3) / 1e12
+    fwd_gate = {"workload": f"fwd B={wg.B} H={wg.H} N={wg.N} d={wg.d} K x3 causal",
+                "ms_median": fms[reps // 2], "tflops": f_gate,
+                "pct_of_bf16_peak": 100.0 * f_gate / peak_burst,
+                "gate": ">= 60% of dense BF16 peak"}
+
+    del gin, go, gl
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": workload_config(w),
+        "pct_of_bf16_peak": 100.0 * value / world / peak_burst,
+        "peak_bf16_tflops": peak_burst, "peak_source": peak_src,
+        "kernel_ms": per, "roofline": roofline, "e2e": e2e,
+        "gpu_launches": 4 * args.steps,
+        "clocks": clk, "forward_gate": fwd_gate,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = oracle_baseline(w, cpu_in)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_only(args, local):
+    """Untimed launches of one part of the path, for profilers: `fwd` runs the
+    forward on the N=8192 d=128 K x3 causal workload, `bwd` runs the backward
+    (prep, main, finish) on the fwd+bwd workload.  W + K launches each."""
+    import torch
+    import exact_tiled_attention_05_gb300 as fa
+    from exact_tiled_attention_05_gb300 import workloads as wl
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    fa.load_library()
+    if args.only == "fwd":
+        w = wl.WORKLOADS[FWD_GATE_WORKLOAD]
+        inp = wl.make_inputs(w, device=dev)
+        o = torch.empty_like(inp["q"])
+        lse = torch.empty(w.B, w.H, w.N, dtype=torch.float32, device=dev)
+        for _ in range(args.warmup + args.steps):
+            fa.forward(inp["q"], inp["k"], inp["v"], causal=True, out=o, lse=lse)
+    else:
+        w = wl.WORKLOADS[WORKLOAD]
+        inp = wl.make_inputs(w, device=dev)
+        o, lse = fa.forward(inp["q"], inp["k"], inp["v"], causal=True)
+        ws = fa.alloc_workspace(w.B, w.H, w.N, w.d, dev)
+        grads = [torch.empty_like(inp["q"]) for _ in range(3)]
+        for _ in range(args.warmup + args.steps):
+            fa.backward(inp["q"], inp["k"], inp["v"], o, lse, inp["do"], causal=True,
+                        dq=grads[0], dk=grads[1], dv=grads[2], workspace=ws)
+    fa.sync_status()
+    print(json.dumps({"only": args.only, "launches": args.warmup + args.steps}), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=("fwd", "bwd"), default=None,
+                    help="untimed launches of one part of the path (for profilers)")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl != "reference" and not args.only:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_setup(args)
+    try:
+        if args.only:
+            run_only(args, local)
+        elif args.impl == "reference":
+            run_reference(args, world, rank)
+        else:
+            run_gpu(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

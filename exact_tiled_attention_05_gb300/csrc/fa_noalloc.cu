@@ -1,0 +1,72 @@
+// fa_noalloc.cu -- a backward pass for callers that cannot allocate device
+// memory.
+//
+// fa_bwd needs a scratch workspace (an fp32 dQ accumulator and the row
+// statistic D) that the caller allocates.  Some callers cannot do that: code
+// that runs where cudaMalloc is unavailable or forbidden (inside a custom
+// allocator's own callbacks, a fixed-footprint embedded service that must not
+// grow its memory after start-up, or a plug-in whose host framework owns every
+// allocation).  fa_bwd_noalloc gives them the same computation with the scratch
+// held in one fixed-size array in this library's device memory.
+//
+// That array lives in every GPU that loads this part of the library and stays
+// there until the process exits.  All calls on a device share it: it keeps the
+// contents of the previous call, the kernels clear what must start at zero
+// (the dQ accumulator is zeroed by the prep stage on every call), and two calls
+// whose work overlaps on the GPU (different streams, or different host threads
+// without ordering) race on it and give wrong results.
+#include <atomic>
+#include <mutex>
+
+#include "../../include/fa.h"
+#include "fa_internal.cuh"
+
+namespace {
+
+// 64 MiB: the fp32 dQ accumulator (4*B*H*N*d bytes) plus D (4*B*H*N bytes),
+// each rounded up to 256 bytes, must fit.
+constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_setup_mutex;
+std::atomic<void*> g_scratch_ptr[kMaxDevices];
+
+// Device address of the scratch array on the current device.  The host-side
+// name g_noalloc_scratch is only a stand-in, so the address is looked up once
+// per device with that device current.
+int scratch_for_current_device(void** out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return FA_ERR_CUDA;
+    if (dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+    void* p = g_scratch_ptr[dev].load(std::memory_order_acquire);
+    if (!p) {
+        std::lock_guard<std::mutex> lock(g_setup_mutex);
+        p = g_scratch_ptr[dev].load(std::memory_order_relaxed);
+        if (!p) {
+            if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p)
+                return FA_ERR_CUDA;
+            g_scratch_ptr[dev].store(p, std::memory_order_release);
+        }
+    }
+    *out = p;
+    return FA_OK;
+}
+
+}  // namespace
+
+extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                              const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                              int B, int H, int N, int d, float scale, int causal, void* stream) {
+    if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
+    const size_t need = fa_bwd_workspace_size(B, H, N, d);
+    if (need == 0) return FA_ERR_INVALID_ARG;
+    if (need > kNoAllocScratchBytes) return FA_ERR_WORKSPACE;  // sizes beyond the fixed scratch
+    void* scratch = nullptr;
+    const int rc = scratch_for_current_device(&scratch);
+    if (rc != FA_OK) return rc;
+    return fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, causal, scratch,
+                  kNoAllocScratchBytes, stream);
+}

@@ -18,7 +18,7 @@
  *  - lse: fp32 [B, H, N], natural logarithm of the row's sum of
  *    exp(scale * q.k) over the visible keys (L = m + log l).
  *  - d (head dimension) is 64 or 128; N >= 1 (any length, tails are masked);
- *    B, H >= 1; B*H*N*d < 2^31.  scale is finite and non-zero (callers usually
+ *    B, H >= 1; B*H*N*d < 2^31.  scale is finite and > 0 (callers usually
  *    pass 1/sqrt(d)); causal is 0 or 1 (key j visible to query i iff j <= i).
  *  - Every pointer is caller-owned device memory; the library keeps no pointer
  *    after a call returns and allocates no device memory per call.
@@ -91,6 +91,23 @@ int fa_bwd_main(const void* q, const void* k, const void* v, const float* lse,
                 void* workspace, size_t workspace_bytes, void* stream);
 int fa_bwd_finish(void* dq, int B, int H, int N, int d,
                   void* workspace, size_t workspace_bytes, void* stream);
+
+/* Backward pass for callers that cannot allocate device memory: code that runs
+ * where cudaMalloc is unavailable or not allowed, such as inside a custom
+ * allocator's own callbacks, a service that must keep a fixed device-memory
+ * footprint after start-up, or a plug-in whose host framework owns every
+ * allocation.  (The pages have no counterpart: this is a packaging choice of
+ * this library.)  Same arguments, results and errors as fa_bwd, minus the workspace: the
+ * scratch (fp32 dQ accumulator + D) lives in one fixed 64 MiB array of library
+ * device memory, so nothing is allocated.  Sizes whose workspace
+ * (fa_bwd_workspace_size) exceeds 64 MiB return FA_ERR_WORKSPACE before any
+ * launch.  The first call on a device looks up the array's device address with
+ * that device current; make that first call before any stream capture.  Every
+ * call on a device shares the array: calls whose work overlaps on the GPU
+ * (other streams, unordered host threads) race on it. */
+int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                   const void* dout, void* dq, void* dk, void* dv,
+                   int B, int H, int N, int d, float scale, int causal, void* stream);
 
 /* Synchronises `stream`, then returns and clears the device status word of the
  * current device: FA_OK, or FA_ERR_DEVICE_TIMEOUT if any kernel gave up on a

@@ -77,7 +77,7 @@ __global__ void __launch_bounds__(256) fa_bwd_finish_kernel(const BwdArgs a, lon
 // warps 4-7 / 8-11 compute for query columns 0-63 / 64-127 of each tile.
 // ---------------------------------------------------------------------------
 constexpr int kBThreads = 384;
-constexpr int kBCompute = 256;
+constexpr int kBCompute = 256;  // threads of warps 4..11; each arrives on the compute barriers
 constexpr int kBBox = 128 * 64 * 2;
 
 template <int HD>
@@ -314,9 +314,9 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             const int s = it % Cfg::kStages;
             const uint32_t ph = (it / Cfg::kStages) & 1;
             const int i = i_begin + it;
-            ok = mbar_wait(smem_u32(&sm.s_full), it & 1, kWaitTimeoutNs, abort) &&
-                 mbar_wait(smem_u32(&sm.qd_full[s]), ph, kWaitTimeoutNs, abort);
-            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            ok = mbar_wait_warp(smem_u32(&sm.s_full), it & 1, kWaitTimeoutNs, abort) &&
+                 mbar_wait_warp(smem_u32(&sm.qd_full[s]), ph, kWaitTimeoutNs, abort);
+            if (!ok) break;
             tc_fence_after();
             float p[64];
             {
@@ -360,9 +360,10 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             tc_fence_before();
             mbar_arrive(smem_u32(&sm.p_ready));
 
-            ok = mbar_wait(smem_u32(&sm.dp_full), it & 1, kWaitTimeoutNs, abort);
-            if (ok && it > 0) ok = mbar_wait(smem_u32(&sm.ds_free), (it - 1) & 1, kWaitTimeoutNs, abort);
-            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            ok = mbar_wait_warp(smem_u32(&sm.dp_full), it & 1, kWaitTimeoutNs, abort);
+            if (ok && it > 0)
+                ok = mbar_wait_warp(smem_u32(&sm.ds_free), (it - 1) & 1, kWaitTimeoutNs, abort);
+            if (!ok) break;
             tc_fence_after();
             const uint32_t d_addr = smem_u32(&sm.delta[s][wg * 64]);
 #pragma unroll
@@ -398,8 +399,8 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             mbar_arrive(smem_u32(&sm.ds_ready));
             mbar_arrive(smem_u32(&sm.qd_empty[s]));
 
-            ok = mbar_wait(smem_u32(&sm.dq_full), it & 1, kWaitTimeoutNs, abort);
-            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            ok = mbar_wait_warp(smem_u32(&sm.dq_full), it & 1, kWaitTimeoutNs, abort);
+            if (!ok) break;
             tc_fence_after();
             {
                 constexpr int kHalf = HD / 2;
@@ -436,8 +437,8 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         if (!ok) {
             if (lane == 0) bwd_timeout(a, abort);
         } else {
-            ok = mbar_wait(smem_u32(&sm.dkdv_done), 0, kWaitTimeoutNs, abort);
-            if (__all_sync(0xffffffffu, ok)) {
+            ok = mbar_wait_warp(smem_u32(&sm.dkdv_done), 0, kWaitTimeoutNs, abort);
+            if (ok) {
                 tc_fence_after();
                 constexpr int kHalf = HD / 2;
                 const bool store = kglob < N;

@@ -35,13 +35,15 @@ constexpr int kBM = 128;        // query rows per Q tile
 constexpr int kBN = 128;        // keys per K/V tile
 constexpr int kThreads = 384;   // 12 warps
 constexpr int kBoxBytes = 128 * 64 * 2;  // one TMA box: 128 rows x 64 bf16
-// The reference max follows the running max exactly (threshold 0).  A stale
-// reference (FA4's conditional rescaling, threshold 8) keeps O / l exact in
-// real arithmetic, but the dominant probability becomes 2^delta instead of
-// exactly 1.0 and picks up bf16 rounding in P; on rows close to one-hot that
-// alone moves O by more than 1e-2.  With an exact max the largest weight of
-// every row is exactly 1.0.
-constexpr float kRescaleThreshold = 0.0f;  // log2 units
+// Conditional rescaling ("FlashAttention 1–4" §"FlashAttention-4"): the
+// reference max m only moves when a tile's max exceeds it by more than 8 (log2
+// units, a factor 256), so most tiles skip the O rescale pass.  P = 2^(s - m)
+// then lies in [0, 256] and its largest entry is no longer exactly 1.0, so the
+// bf16 rounding of P would bias O on rows close to one-hot.  Two row sums fix
+// that: O is normalised by the sum of the bf16 weights the MMA actually used
+// (the rounding of the dominant weight cancels in the ratio), and lse uses the
+// fp32 sum of the unrounded weights.
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 template <int HD>
 struct FwdCfg {
@@ -257,21 +259,28 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
         const int t = (warp - 4) >> 2;
         const int wq = warp & 3;  // TMEM lane quarter this warp may access
         const int row = wq * 32 + lane;
-        const int qi = q0[t] + row;
+        const int my_q0 = t == 0 ? q0[0] : q0[1];
+        const int my_nkv = t == 0 ? nkv[0] : nkv[1];
+        const int qi = my_q0 + row;
         const uint32_t lane_addr = tbase + (static_cast<uint32_t>(wq * 32) << 16);
         const uint32_t s_addr = lane_addr + (static_cast<uint32_t>(t) * Cfg::kSColStride);
         const uint32_t o_addr = lane_addr + Cfg::kOCol0 + t * HD;
         const float sl2 = args.scale_log2;
-        float m_ref = -INFINITY;  // reference max, log2 units
-        float l_sum = 0.f;
+        float m_ref = -INFINITY;  // running max, log2 units
+        uint64_t l_pair = f2_pack(0.f, 0.f);   // sum of fp32 weights (for lse), two partial sums
+        uint64_t lr_pair = f2_pack(0.f, 0.f);  // sum of the bf16 weights (normalises O)
+        const uint64_t sl2_pair = f2_pack(sl2, sl2);
         bool ok = true;
-        for (int j = 0; j < nkv[t]; ++j) {
-            ok = mbar_wait(smem_u32(&sm.s_full[t]), j & 1, kWaitTimeoutNs, abort);
-            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        for (int j = 0; j < my_nkv; ++j) {
+            ok = mbar_wait_warp(smem_u32(&sm.s_full[t]), j & 1, kWaitTimeoutNs, abort);
+            if (!ok) break;
             tc_fence_after();
-            float s[kBN];
+            uint32_t sr[kBN];
             {
-                uint32_t r0[32], r1[32], r2[32], r3[32];
+                uint32_t(&r0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[0]);
+                uint32_t(&r1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[32]);
+                uint32_t(&r2)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[64]);
+                uint32_t(&r3)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[96]);
                 tmem_ld32(s_addr + 0, r0);
                 tmem_ld32(s_addr + 32, r1);
                 tmem_ld32(s_addr + 64, r2);
@@ -281,27 +290,27 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                 reg_fence(r1);
                 reg_fence(r2);
                 reg_fence(r3);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    s[i] = __uint_as_float(r0[i]);
-                    s[32 + i] = __uint_as_float(r1[i]);
-                    s[64 + i] = __uint_as_float(r2[i]);
-                    s[96 + i] = __uint_as_float(r3[i]);
-                }
             }
             const int kbase = j * kBN;
-            const bool edge = (kbase + kBN > N) || (args.causal && kbase + kBN - 1 > q0[t]);
+            const bool edge = (kbase + kBN > N) || (args.causal && kbase + kBN - 1 > my_q0);
             if (edge) {
                 const int kend = args.causal ? min(N, qi + 1) : N;
 #pragma unroll
                 for (int c = 0; c < kBN; ++c)
-                    if (kbase + c >= kend) s[c] = -INFINITY;
+                    if (kbase + c >= kend) sr[c] = __float_as_uint(-INFINITY);
             }
-            float mx = s[0];
+            // row max: four independent chains of 3-input max
+            float mc[4];
 #pragma unroll
-            for (int c = 1; c < kBN; ++c) mx = fmaxf(mx, s[c]);
-            const float mx2 = mx * sl2;
-            // reference-max update (conditional rescaling)
+            for (int g = 0; g < 4; ++g) mc[g] = __uint_as_float(sr[g]);
+#pragma unroll
+            for (int c = 4; c < kBN; c += 8) {
+#pragma unroll
+                for (int g = 0; g < 4; ++g)
+                    mc[g] = fmax3(mc[g], __uint_as_float(sr[c + g]), __uint_as_float(sr[c + 4 + g]));
+            }
+            const float mx2 = fmax3(mc[0], mc[1], fmaxf(mc[2], mc[3])) * sl2;
+            // running-max update; O and l are rescaled when the max rises
             bool rescale = false;
             float alpha = 1.f;
             if (m_ref == -INFINITY) {
@@ -309,14 +318,16 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
             } else if (mx2 > m_ref + kRescaleThreshold) {
                 rescale = true;
                 alpha = ex2(m_ref - mx2);
-                l_sum *= alpha;
+                l_pair = f2_mul(l_pair, f2_pack(alpha, alpha));
+                lr_pair = f2_mul(lr_pair, f2_pack(alpha, alpha));
                 m_ref = mx2;
             }
             if (__any_sync(0xffffffffu, rescale)) {
-                // O already holds PV of earlier tiles: wait for the latest one.
-                ok = mbar_wait(smem_u32(&sm.o_done[t]), (j - 1) & 1, kWaitTimeoutNs, abort);
-                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                // O already holds P V of earlier tiles: wait for the latest one.
+                ok = mbar_wait_warp(smem_u32(&sm.o_done[t]), (j - 1) & 1, kWaitTimeoutNs, abort);
+                if (!ok) break;
                 tc_fence_after();
+                const uint64_t a2 = f2_pack(alpha, alpha);
                 uint32_t r[32];
 #pragma unroll 1
                 for (int c = 0; c < HD / 32; ++c) {
@@ -324,23 +335,30 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                     tmem_wait_ld();
                     reg_fence(r);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                    for (int i = 0; i < 16; ++i) {
+                        const float2 v = f2_unpack(f2_mul(f2_pack_u(r[2 * i], r[2 * i + 1]), a2));
+                        r[2 * i] = __float_as_uint(v.x);
+                        r[2 * i + 1] = __float_as_uint(v.y);
+                    }
                     tmem_st32(o_addr + c * 32, r);
                 }
                 tmem_wait_st();
             }
             const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
+            const uint64_t negm_pair = f2_pack(neg_m, neg_m);
             // P = exp2(s * scale * log2e - m), packed bf16 pairs over S columns [0, 64)
 #pragma unroll
             for (int c = 0; c < kBN / 32; ++c) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const float p0 = ex2(fmaf(s[c * 32 + 2 * i], sl2, neg_m));
-                    const float p1 = ex2(fmaf(s[c * 32 + 2 * i + 1], sl2, neg_m));
-                    l_sum += p0 + p1;
+                    const int e = c * 32 + 2 * i;
+                    const float2 x = f2_unpack(f2_fma(f2_pack_u(sr[e], sr[e + 1]), sl2_pair, negm_pair));
+                    const float p0 = ex2(x.x);
+                    const float p1 = ex2(x.y);
+                    l_pair = f2_add(l_pair, f2_pack(p0, p1));
                     pk[i] = pack_bf16x2(p0, p1);
+                    lr_pair = f2_add(lr_pair, f2_pack_u(pk[i] << 16, pk[i] & 0xffff0000u));
                 }
                 tmem_st16(s_addr + c * 16, pk);
             }
@@ -348,13 +366,17 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
             tc_fence_before();
             mbar_arrive(smem_u32(&sm.p_full[t]));
         }
+        const float2 l_parts = f2_unpack(l_pair);
+        const float l_sum = l_parts.x + l_parts.y;
+        const float2 lr_parts = f2_unpack(lr_pair);
+        const float l_round = lr_parts.x + lr_parts.y;
         if (!ok) {
             if (lane == 0) record_timeout(args, abort);
-        } else if (nkv[t] > 0) {
-            ok = mbar_wait(smem_u32(&sm.o_done[t]), (nkv[t] - 1) & 1, kWaitTimeoutNs, abort);
-            if (__all_sync(0xffffffffu, ok)) {
+        } else if (my_nkv > 0) {
+            ok = mbar_wait_warp(smem_u32(&sm.o_done[t]), (my_nkv - 1) & 1, kWaitTimeoutNs, abort);
+            if (ok) {
                 tc_fence_after();
-                const float inv_l = 1.f / l_sum;
+                const float inv_l = 1.f / l_round;
                 const bool store = qi < N;
                 const size_t row_off = (static_cast<size_t>(bh) * N + qi) * HD;
                 uint8_t* orow = reinterpret_cast<uint8_t*>(args.o) + row_off * 2;

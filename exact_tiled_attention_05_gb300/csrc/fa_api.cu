@@ -88,6 +88,23 @@ int make_map(CUtensorMap* map, const void* ptr, int BH, int N, int d) {
     return r == CUDA_SUCCESS ? kOk : kErrCuda;
 }
 
+// fp32 [BH, N, d] accumulator -> 3-D map, box 32 x 128 x 1 (128-byte rows),
+// 128 B swizzle: the layout the dQ reduce stages in shared memory.
+int make_map_f32(CUtensorMap* map, const void* ptr, int BH, int N, int d) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return kErrCuda;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                          static_cast<cuuint64_t>(BH)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4,
+                             static_cast<cuuint64_t>(d) * 4 * static_cast<cuuint64_t>(N)};
+    cuuint32_t box[3] = {32, 128, 1};
+    cuuint32_t elem[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(ptr), dims,
+                     strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? kOk : kErrCuda;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int check_shape(int B, int H, int N, int d, float scale, int causal) {
@@ -218,12 +235,14 @@ int fa_bwd_main(const void* q, const void* k, const void* v, const float* lse, c
     a.dout = dout;
     a.dk = dk;
     a.dv = dv;
-    CUtensorMap tq, tk, tv, tdo;
+    CUtensorMap tq, tk, tv, tdo, tdq;
     const int BH = B * H;
     if ((rc = make_map(&tq, q, BH, N, d)) || (rc = make_map(&tk, k, BH, N, d)) ||
-        (rc = make_map(&tv, v, BH, N, d)) || (rc = make_map(&tdo, dout, BH, N, d)))
+        (rc = make_map(&tv, v, BH, N, d)) || (rc = make_map(&tdo, dout, BH, N, d)) ||
+        (rc = make_map_f32(&tdq, a.dq_acc, BH, N, d)))
         return rc;
-    return map_cuda(launch_bwd_main(d, tq, tk, tv, tdo, a, static_cast<cudaStream_t>(stream)));
+    return map_cuda(
+        launch_bwd_main(d, tq, tk, tv, tdo, tdq, a, static_cast<cudaStream_t>(stream)));
 }
 
 int fa_bwd_finish(void* dq, int B, int H, int N, int d, void* workspace, size_t workspace_bytes,

@@ -108,7 +108,8 @@ struct alignas(1024) BwdSmem {
     uint64_t kv_full;
     uint64_t qd_full[BwdCfg<HD>::kStages];
     uint64_t qd_empty[BwdCfg<HD>::kStages];
-    uint64_t s_full, dp_full, p_ready, ds_ready, ds_free, dq_full, dq_drained, dkdv_done, drain;
+    uint64_t s_full, dp_full, p_ready, ds_ready, ds_free, dq_full, dq_drained, dq_staged, dkdv_done,
+        drain;
     uint32_t tmem_base;
     int abort;
 };
@@ -125,7 +126,7 @@ template <int HD>
 __global__ void __launch_bounds__(kBThreads, 1)
 fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
-                   const BwdArgs a) {
+                   const __grid_constant__ CUtensorMap tdq, const BwdArgs a) {
     using Cfg = BwdCfg<HD>;
     extern __shared__ __align__(1024) uint8_t bsmem_raw[];
     if ((smem_u32(bsmem_raw) & 1023u) != 0u) {  // the swizzled layouts need 1 KB alignment
@@ -154,7 +155,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         mbar_init(smem_u32(&sm.kv_full), 1);
         for (int s = 0; s < Cfg::kStages; ++s) {
             mbar_init(smem_u32(&sm.qd_full[s]), 2);
-            mbar_init(smem_u32(&sm.qd_empty[s]), 1 + kBCompute);
+            mbar_init(smem_u32(&sm.qd_empty[s]), 1);  // the dQ reducer frees the stage
         }
         mbar_init(smem_u32(&sm.s_full), 1);
         mbar_init(smem_u32(&sm.dp_full), 1);
@@ -163,6 +164,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         mbar_init(smem_u32(&sm.ds_free), 1);
         mbar_init(smem_u32(&sm.dq_full), 1);
         mbar_init(smem_u32(&sm.dq_drained), kBCompute);
+        mbar_init(smem_u32(&sm.dq_staged), kBCompute);
         mbar_init(smem_u32(&sm.dkdv_done), 1);
         mbar_init(smem_u32(&sm.drain), 1);
         fence_mbar_init();
@@ -292,12 +294,37 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                 }
                 umma_commit(smem_u32(&sm.dq_full));
                 umma_commit(smem_u32(&sm.ds_free));
-                umma_commit(smem_u32(&sm.qd_empty[s]));
             }
             if (!ok) bwd_timeout(a, abort);
             umma_commit(smem_u32(&sm.dkdv_done));
             umma_commit(smem_u32(&sm.drain));
             mbar_wait(smem_u32(&sm.drain), 0, kWaitTimeoutNs, abort);
+        }
+    } else if (warp == 3) {
+        // ===================== dQ reducer =====================
+        // Adds each staged dQ tile into the fp32 accumulator with TMA bulk
+        // reduce-add (whole 128-byte lines instead of per-thread atomics), then
+        // hands the stage back to the loader once TMA has read it.
+        if (elect_one()) {
+            constexpr int kBoxes = HD / 32;
+            tma_prefetch_desc(&tdq);
+            bool ok = true;
+            for (int it = 0; ok && it < niter; ++it) {
+                const int s = it % Cfg::kStages;
+                const int i = i_begin + it;
+                if (!(ok = mbar_wait(smem_u32(&sm.dq_staged), it & 1, kWaitTimeoutNs, abort))) break;
+#pragma unroll
+                for (int b = 0; b < kBoxes; ++b) {
+                    const uint32_t box = (b < kBoxes / 2 ? smem_u32(sm.q[s]) : smem_u32(sm.dout[s])) +
+                                         (b % (kBoxes / 2)) * 16384;
+                    tma_reduce_add_3d(&tdq, box, b * 32, i * 128, bh);
+                }
+                bulk_commit_group();
+                bulk_wait_group_read0();
+                mbar_arrive(smem_u32(&sm.qd_empty[s]));
+            }
+            if (!ok) bwd_timeout(a, abort);
+            bulk_wait_group0();  // every reduction has landed before the CTA exits
         }
     } else if (warp >= 4) {
         // ===================== compute =====================
@@ -308,7 +335,6 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         const uint32_t lane_addr = tbase + (static_cast<uint32_t>(wq * 32) << 16);
         const float sl2 = a.scale_log2;
         const uint32_t ds_row = smem_u32(sm.ds) + wg * kBBox + row * 128;
-        float* dq_acc_head = a.dq_acc + static_cast<size_t>(bh) * N * HD;
         bool ok = true;
         for (int it = 0; it < niter; ++it) {
             const int s = it % Cfg::kStages;
@@ -397,7 +423,6 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(smem_u32(&sm.ds_ready));
-            mbar_arrive(smem_u32(&sm.qd_empty[s]));
 
             ok = mbar_wait_warp(smem_u32(&sm.dq_full), it & 1, kWaitTimeoutNs, abort);
             if (!ok) break;
@@ -423,15 +448,27 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                     tc_fence_before();
                     mbar_arrive(smem_u32(&sm.dq_drained));
                 }
-                const int qrow = i * 128 + row;
-                if (qrow < N) {
-                    float* dst = dq_acc_head + static_cast<size_t>(qrow) * HD + wg * kHalf;
-                    const float sc = a.scale;
+                // Stage scale * dQ in the Q/dO buffers of this iteration (every MMA
+                // that read them has completed): 32-column fp32 boxes, 128-byte
+                // swizzle, boxes [0, nb/2) in q[s] and [nb/2, nb) in dout[s].
+                constexpr int kBoxes = HD / 32;
+                const uint64_t sc2 = f2_pack(a.scale, a.scale);
 #pragma unroll
-                    for (int c = 0; c < kHalf; c += 4)
-                        red_add_v4_f32(dst + c, sc * __uint_as_float(r[c]), sc * __uint_as_float(r[c + 1]),
-                                       sc * __uint_as_float(r[c + 2]), sc * __uint_as_float(r[c + 3]));
+                for (int bl = 0; bl < kHalf / 32; ++bl) {
+                    const int b = wg * (kHalf / 32) + bl;
+                    const uint32_t box = (b < kBoxes / 2 ? smem_u32(sm.q[s]) : smem_u32(sm.dout[s])) +
+                                         (b % (kBoxes / 2)) * 16384 + row * 128;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const int e = bl * 32 + c * 4;
+                        const float2 v0 = f2_unpack(f2_mul(f2_pack_u(r[e], r[e + 1]), sc2));
+                        const float2 v1 = f2_unpack(f2_mul(f2_pack_u(r[e + 2], r[e + 3]), sc2));
+                        st_shared_v4(box + ((c ^ (row & 7)) << 4), __float_as_uint(v0.x),
+                                     __float_as_uint(v0.y), __float_as_uint(v1.x), __float_as_uint(v1.y));
+                    }
                 }
+                fence_proxy_async_smem();
+                mbar_arrive(smem_u32(&sm.dq_staged));
             }
         }
         if (!ok) {
@@ -486,14 +523,15 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
 
 template <int HD>
 cudaError_t launch_bwd_main_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                              const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t stream) {
+                              const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a,
+                              cudaStream_t stream) {
     const size_t smem = sizeof(BwdSmem<HD>);
     cudaError_t e = cudaFuncSetAttribute(fa_bwd_main_kernel<HD>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     const unsigned grid = static_cast<unsigned>(a.n_kblk) * static_cast<unsigned>(a.BH);
-    fa_bwd_main_kernel<HD><<<grid, kBThreads, smem, stream>>>(tq, tk, tv, tdo, a);
+    fa_bwd_main_kernel<HD><<<grid, kBThreads, smem, stream>>>(tq, tk, tv, tdo, tdq, a);
     return cudaGetLastError();
 }
 
@@ -524,10 +562,10 @@ cudaError_t launch_bwd_finish(int d, const BwdArgs& a, cudaStream_t stream) {
 }
 
 cudaError_t launch_bwd_main(int d, const CUtensorMap& tq, const CUtensorMap& tk,
-                            const CUtensorMap& tv, const CUtensorMap& tdo, const BwdArgs& a,
-                            cudaStream_t stream) {
-    if (d == 64) return launch_bwd_main_t<64>(tq, tk, tv, tdo, a, stream);
-    return launch_bwd_main_t<128>(tq, tk, tv, tdo, a, stream);
+                            const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
+                            const BwdArgs& a, cudaStream_t stream) {
+    if (d == 64) return launch_bwd_main_t<64>(tq, tk, tv, tdo, tdq, a, stream);
+    return launch_bwd_main_t<128>(tq, tk, tv, tdo, tdq, a, stream);
 }
 
 }  // namespace fa

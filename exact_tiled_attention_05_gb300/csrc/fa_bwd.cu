@@ -141,8 +141,16 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     const int nq = a.n_kblk;  // query tiles == key tiles (both 128 rows)
     int bh, j;
     if (a.causal) {
-        j = static_cast<int>(blockIdx.x) / a.BH;
-        bh = static_cast<int>(blockIdx.x) % a.BH;
+        // groups of a.group heads; inside a group the key blocks with the most
+        // query tiles (small j) launch first.  Keeping few heads in flight keeps
+        // their Q, dO and fp32 dQ accumulator resident in L2.
+        const int b = static_cast<int>(blockIdx.x);
+        const int grp = b / (a.group * a.n_kblk);
+        const int first = grp * a.group;
+        const int gc = min(a.group, a.BH - first);
+        const int r = b - grp * a.group * a.n_kblk;
+        j = r / gc;
+        bh = first + r % gc;
     } else {
         bh = static_cast<int>(blockIdx.x) / a.n_kblk;
         j = static_cast<int>(blockIdx.x) % a.n_kblk;

@@ -93,11 +93,20 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
     const int N = args.N;
     const int BH = args.BH;
 
-    // ---- work unit: (head, 256-row query block); heavy causal blocks first ----
+    // ---- work unit: (head, 256-row query block) ----
+    // Causal: heads are taken in groups of args.group; inside a group the
+    // heaviest query blocks (the longest key ranges) launch first, so the
+    // block scheduler approximates longest-processing-time-first while the
+    // K/V of the heads in flight stay in L2.
     int bh, qb;
     if (args.causal) {
-        qb = args.n_qblk - 1 - static_cast<int>(blockIdx.x) / BH;
-        bh = static_cast<int>(blockIdx.x) % BH;
+        const int b = static_cast<int>(blockIdx.x);
+        const int grp = b / (args.group * args.n_qblk);
+        const int first = grp * args.group;
+        const int gc = min(args.group, BH - first);
+        const int r = b - grp * args.group * args.n_qblk;
+        qb = args.n_qblk - 1 - r / gc;
+        bh = first + r % gc;
     } else {
         bh = static_cast<int>(blockIdx.x) / args.n_qblk;
         qb = static_cast<int>(blockIdx.x) % args.n_qblk;

@@ -29,6 +29,7 @@ struct FwdArgs {
     int BH;
     int N;
     int n_qblk;       // query blocks (256 rows each) per head
+    int group;        // causal launch order: heads per group (heavy blocks first within a group)
     int causal;
     float scale_log2; // scale * log2(e)
     int* status;      // device status word
@@ -49,6 +50,7 @@ struct BwdArgs {
     int BH;
     int N;
     int n_kblk;       // key blocks (128 rows) per head
+    int group;        // causal launch order: heads per group (heavy blocks first within a group)
     int causal;
     float scale;
     float scale_log2;

@@ -39,6 +39,34 @@ def fwd_flops(w, causal=True):
     return 4.0 * w.B * w.H * w.N * w.N * w.d / (2.0 if causal else 1.0)
 
 
+KERNEL_SOURCES = {"fa_bwd_main_kernel<128>": ("fa_bwd.cu", "ptx.cuh", "fa_internal.cuh"),
+                  "fa_fwd_kernel<128>": ("fa_fwd.cu", "ptx.cuh", "fa_internal.cuh")}
+
+
+def profiled_traffic(kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or None
+    when no capture exists or the kernel's sources changed since it was taken."""
+    import glob
+    import hashlib
+    srcs = KERNEL_SOURCES.get(kernel)
+    if not srcs:
+        return None
+    h = hashlib.sha256()
+    for f in srcs:
+        with open(os.path.join(ROOT, "exact_tiled_attention_05_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    sha = h.hexdigest()
+    for path in glob.glob(os.path.join(ROOT, "profiles", "*.md")):
+        with open(path) as fh:
+            for line in fh:
+                if not line.startswith("bench-traffic:"):
+                    continue
+                fields = dict(kv.split("=", 1) for kv in line.split()[1:])
+                if fields.get("kernel") == kernel and fields.get("source_sha256") == sha:
+                    return int(fields["bytes"])
+    return None
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -173,7 +201,7 @@ def run_reference(args, world, rank):
     # chosen so the whole run stays within about two minutes.
     full = wl.make_inputs(w, B=1, H=1)
     bits = {nm: wl.bf16_bits(t) for nm, t in full.items()}
-    budget = 120.0 / max(1, args.steps + args.warmup)
+    budget = args.ref_budget_s / max(1, args.steps + args.warmup)
 
     def run_prefix(n):
         sl = {nm: b[:, :n].copy() for nm, b in bits.items()}
@@ -308,10 +336,19 @@ def run_gpu(args, world, rank, local):
         "peak_kind": f"bf16_tflops_sustained ({peak_src}), the kernel runs inside a long step loop",
         "frac_of_burst_peak": achieved / peak_burst if achieved else None,
         "traffic": None,
-        "traffic_note": "ncu dram bytes per launch are summarised under profiles/",
+        "traffic_note": "dram__bytes_read.sum + dram__bytes_write.sum per launch from the committed "
+                        "ncu capture under profiles/; null when the kernel changed since",
         "flops_per_launch": dom_flops,
         "ms_per_launch": per[dom],
     }
+
+    kname = roofline["kernel"]
+    roofline["traffic"] = profiled_traffic(kname)
+    if roofline["traffic"] is not None:
+        alg = {"fa_bwd_main_kernel<128>": (16 * w.N * w.d + 12 * w.N) * w.B * w.H,
+               "fa_fwd_kernel<128>": (8 * w.N * w.d + 4 * w.N) * w.B * w.H}.get(kname)
+        roofline["algorithmic_bytes"] = alg
+        roofline["traffic_over_algorithmic"] = roofline["traffic"] / alg if alg else None
 
     # ---------------- end to end through the public API, host buffers ----------------
     pin = {n: t.pin_memory() for n, t in cpu_in.items()}
@@ -392,21 +429,23 @@ def run_gpu(args, world, rank, local):
 
 def run_only(args, local):
     """Untimed launches of one part of the path, for profilers: `fwd` runs the
-    forward on the N=8192 d=128 K x3 causal workload, `bwd` runs the backward
-    (prep, main, finish) on the fwd+bwd workload.  W + K launches each."""
+    forward on the N=8192 d=128 K x3 causal workload, `fwd64` the non-causal
+    forward on B=4 H=16 N=2048 d=64, `bwd` the backward (prep, main, finish)
+    on the fwd+bwd workload.  W + K launches each."""
     import torch
     import exact_tiled_attention_05_gb300 as fa
     from exact_tiled_attention_05_gb300 import workloads as wl
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     fa.load_library()
-    if args.only == "fwd":
-        w = wl.WORKLOADS[FWD_GATE_WORKLOAD]
+    if args.only in ("fwd", "fwd64"):
+        w = wl.WORKLOADS[FWD_GATE_WORKLOAD if args.only == "fwd" else "fwd_2k_d64"]
+        causal = args.only == "fwd"
         inp = wl.make_inputs(w, device=dev)
         o = torch.empty_like(inp["q"])
         lse = torch.empty(w.B, w.H, w.N, dtype=torch.float32, device=dev)
         for _ in range(args.warmup + args.steps):
-            fa.forward(inp["q"], inp["k"], inp["v"], causal=True, out=o, lse=lse)
+            fa.forward(inp["q"], inp["k"], inp["v"], causal=causal, out=o, lse=lse)
     else:
         w = wl.WORKLOADS[WORKLOAD]
         inp = wl.make_inputs(w, device=dev)
@@ -427,7 +466,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=("fwd", "bwd"), default=None,
+    ap.add_argument("--ref-budget-s", type=float, default=120.0,
+                    help="--impl reference: seconds of oracle work for the whole run")
+    ap.add_argument("--only", choices=("fwd", "fwd64", "bwd"), default=None,
                     help="untimed launches of one part of the path (for profilers)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl != "reference" and not args.only:

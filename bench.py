@@ -351,40 +351,71 @@ def run_gpu(args, world, rank, local):
         roofline["traffic_over_algorithmic"] = roofline["traffic"] / alg if alg else None
 
     # ---------------- end to end through the public API, host buffers ----------------
+    # Every step copies its inputs in from pinned host memory and its results
+    # (O, lse, dQ, dK, dV) back out.  Steps are pipelined over three streams with
+    # two sets of device buffers: step k's copy-in and step k-1's copy-out
+    # overlap step k-1's / k's compute.
+    nbuf = 2
     pin = {n: t.pin_memory() for n, t in cpu_in.items()}
-    out_host = {n: torch.empty(t.shape, dtype=t.dtype).pin_memory() for n, t in
-                (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
+    dev_in = [{n: torch.empty_like(t, device=dev) for n, t in cpu_in.items()} for _ in range(nbuf)]
+    dev_out = [{"o": torch.empty_like(o), "lse": torch.empty_like(lse), "dq": torch.empty_like(dq),
+                "dk": torch.empty_like(dk), "dv": torch.empty_like(dv)} for _ in range(nbuf)]
+    host_out = [{n: torch.empty(t.shape, dtype=t.dtype).pin_memory() for n, t in d_.items()}
+                for d_ in dev_out]
     h2d = sum(t.numel() * t.element_size() for t in pin.values())
-    d2h = sum(t.numel() * t.element_size() for t in out_host.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out[0].values())
     e2e_steps = max(1, min(args.steps, 50))
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    s_cmp = stream
+    in_done = [torch.cuda.Event() for _ in range(nbuf)]
+    cmp_done = [torch.cuda.Event() for _ in range(nbuf)]
+    out_done = [torch.cuda.Event() for _ in range(nbuf)]
 
-    def e2e_step():
-        q.copy_(pin["q"], non_blocking=True)
-        k.copy_(pin["k"], non_blocking=True)
-        v.copy_(pin["v"], non_blocking=True)
-        do.copy_(pin["do"], non_blocking=True)
-        fa.forward(q, k, v, scale=scale, causal=True, out=o, lse=lse)
-        fa.backward(q, k, v, o, lse, do, scale=scale, causal=True, dq=dq, dk=dk, dv=dv,
-                    workspace=ws)
-        for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
-            out_host[n].copy_(t, non_blocking=True)
+    def e2e_run(nsteps):
+        for kstep in range(nsteps):
+            b = kstep % nbuf
+            if kstep >= nbuf:
+                s_in.wait_event(cmp_done[b])   # step k-2 no longer reads these inputs
+            with torch.cuda.stream(s_in):
+                for n in ("q", "k", "v", "do"):
+                    dev_in[b][n].copy_(pin[n], non_blocking=True)
+                in_done[b].record(s_in)
+            s_cmp.wait_event(in_done[b])
+            if kstep >= nbuf:
+                s_cmp.wait_event(out_done[b])  # step k-2's results have left the device
+            x, y = dev_in[b], dev_out[b]
+            fa.forward(x["q"], x["k"], x["v"], scale=scale, causal=True, out=y["o"], lse=y["lse"],
+                       stream=s_cmp)
+            fa.backward(x["q"], x["k"], x["v"], y["o"], y["lse"], x["do"], scale=scale, causal=True,
+                        dq=y["dq"], dk=y["dk"], dv=y["dv"], workspace=ws, stream=s_cmp)
+            cmp_done[b].record(s_cmp)
+            s_out.wait_event(cmp_done[b])
+            with torch.cuda.stream(s_out):
+                for n, t in y.items():
+                    host_out[b][n].copy_(t, non_blocking=True)
+                out_done[b].record(s_out)
 
-    e2e_step()
+    e2e_run(nbuf)
     torch.cuda.synchronize(dev)
     barrier(world)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
+    e0.record(s_in)
+    s_cmp.wait_event(e0)
+    s_out.wait_event(e0)
+    e2e_run(e2e_steps)
+    s_out.wait_event(cmp_done[(e2e_steps - 1) % nbuf])
+    e1.record(s_out)
     torch.cuda.synchronize(dev)
     barrier(world)
     check(fa.fa_sync_status(h), "e2e")
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     e2e = {"value": f_step * e2e_steps * world / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-           "ms_per_step": e2e_ms / e2e_steps}
+           "ms_per_step": e2e_ms / e2e_steps,
+           "pipeline": "copy-in, compute and copy-out on three streams, two buffer sets",
+           "gpu_launches": 4 * e2e_steps}
+    del dev_in, dev_out
 
     # ---------------- forward gate: N = 8192, d = 128, causal ----------------
     wg = wl.WORKLOADS[FWD_GATE_WORKLOAD]

@@ -46,17 +46,22 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(p) > t for p in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
-    """Compile and link libfa.so if any source is newer than it; return its path."""
+def build(force: bool = False, verbose: bool = False, extra_flags=None, lib_path=None,
+          build_dir=None) -> str:
+    """Compile and link libfa.so if any source is newer than it; return its path.
+    lib_path / build_dir / extra_flags build a variant elsewhere (the tests use
+    this for a fault-injection build)."""
+    lib_path = lib_path or LIB_PATH
+    build_dir = build_dir or BUILD_DIR
     deps = _deps()
-    if not force and not _stale(LIB_PATH, deps):
-        return LIB_PATH
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    if not force and not _stale(lib_path, deps):
+        return lib_path
+    os.makedirs(build_dir, exist_ok=True)
     nvcc = _nvcc()
     flags = NVCC_FLAGS + list(extra_flags or [])
 
     def compile_one(src):
-        obj = os.path.join(BUILD_DIR, os.path.splitext(src)[0] + ".o")
+        obj = os.path.join(build_dir, os.path.splitext(src)[0] + ".o")
         cmd = [nvcc, *ARCH, *flags, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
@@ -69,13 +74,13 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
 
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

@@ -216,7 +216,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             }
             const int i = i_begin + it;
             const uint32_t fbar = smem_u32(&sm.qd_full[s]);
-            if (leader) {
+            if (leader && !FA_FAULT_INJECT) {
                 mbar_arrive_expect_tx(fbar, 2 * Cfg::kTile);
                 for (int b = 0; b < Cfg::kBoxes; ++b) {
                     tma_load_3d(smem_u32(sm.q[s] + b * kBBox), &tq, fbar, b * 64, i * 128, bh);
@@ -234,11 +234,12 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             ++issued;
         }
         if (leader) {
-            for (int s = 0; s < Cfg::kStages && s < issued; ++s) {
+            // Let every copy that was issued land before the CTA can exit.
+            for (int s = 0; !FA_FAULT_INJECT && s < Cfg::kStages && s < issued; ++s) {
                 const int last = s + Cfg::kStages * ((issued - 1 - s) / Cfg::kStages);
-                mbar_wait(smem_u32(&sm.qd_full[s]), (last / Cfg::kStages) & 1, kWaitTimeoutNs, abort);
+                mbar_wait_drain(smem_u32(&sm.qd_full[s]), (last / Cfg::kStages) & 1, kWaitTimeoutNs);
             }
-            mbar_wait(smem_u32(&sm.kv_full), 0, kWaitTimeoutNs, abort);
+            mbar_wait_drain(smem_u32(&sm.kv_full), 0, kWaitTimeoutNs);
         }
     } else if (warp == 1) {
         // ===================== MMA issuer =====================
@@ -306,7 +307,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             if (!ok) bwd_timeout(a, abort);
             umma_commit(smem_u32(&sm.dkdv_done));
             umma_commit(smem_u32(&sm.drain));
-            mbar_wait(smem_u32(&sm.drain), 0, kWaitTimeoutNs, abort);
+            mbar_wait_drain(smem_u32(&sm.drain), 0, kWaitTimeoutNs);
         }
     } else if (warp == 3) {
         // ===================== dQ reducer =====================

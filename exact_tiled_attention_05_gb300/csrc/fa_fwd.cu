@@ -165,7 +165,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                     tma_load_3d(smem_u32(sm.q[t] + b * kBoxBytes), &tq, qbar, b * 64, q0[t], bh);
             }
             int issued = 0;
-            for (int idx = 0; idx < 2 * nmax; ++idx) {
+            const int n_loads = FA_FAULT_INJECT ? 0 : 2 * nmax;
+            for (int idx = 0; idx < n_loads; ++idx) {
                 const int slot = idx % Cfg::kStages;
                 const uint32_t ph = (idx / Cfg::kStages) & 1;
                 if (!mbar_wait(smem_u32(&sm.kv_empty[slot]), ph ^ 1, kWaitTimeoutNs, abort)) {
@@ -183,10 +184,10 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
             // Let every copy that was issued land before the CTA can exit.
             for (int slot = 0; slot < Cfg::kStages && slot < issued; ++slot) {
                 const int last = slot + Cfg::kStages * ((issued - 1 - slot) / Cfg::kStages);
-                mbar_wait(smem_u32(&sm.kv_full[slot]), (last / Cfg::kStages) & 1, kWaitTimeoutNs,
-                          abort);
+                mbar_wait_drain(smem_u32(&sm.kv_full[slot]), (last / Cfg::kStages) & 1,
+                                kWaitTimeoutNs);
             }
-            mbar_wait(qbar, 0, kWaitTimeoutNs, abort);
+            mbar_wait_drain(qbar, 0, kWaitTimeoutNs);
         }
     } else if (warp == 1) {
         // ===================== MMA issuer =====================
@@ -261,7 +262,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
             if (!ok) record_timeout(args, abort);
             // Every MMA (and every commit before it) completes before the CTA leaves.
             umma_commit(smem_u32(&sm.drain));
-            mbar_wait(smem_u32(&sm.drain), 0, kWaitTimeoutNs, abort);
+            mbar_wait_drain(smem_u32(&sm.drain), 0, kWaitTimeoutNs);
         }
     } else if (warp >= 4) {
         // ===================== softmax / epilogue =====================

@@ -20,8 +20,20 @@ enum : int {
     kErrDeviceTimeout = 6,
 };
 
-// A kernel that waits longer than this on one barrier gives up.
-constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
+// A kernel that waits longer than this on one barrier gives up.  A test build
+// may shorten it.
+#ifndef FA_WAIT_TIMEOUT_NS
+#define FA_WAIT_TIMEOUT_NS 2000000000ull
+#endif
+constexpr uint64_t kWaitTimeoutNs = FA_WAIT_TIMEOUT_NS;
+
+// Test builds only (never set by the library build): with FA_FAULT_INJECT=1 the
+// load warps never issue their K/V (forward) or Q/dO (backward) copies, so a
+// bounded wait runs out and the kernel must report FA_ERR_DEVICE_TIMEOUT and
+// leave cleanly.  No fault, trap or endless wait is involved.
+#ifndef FA_FAULT_INJECT
+#define FA_FAULT_INJECT 0
+#endif
 
 struct FwdArgs {
     void* o;          // bf16 [BH, N, d]

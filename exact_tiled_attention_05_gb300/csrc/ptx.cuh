@@ -87,6 +87,19 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
     }
 }
 
+// Wait used when draining before exit: copies and MMAs already in flight must
+// land before the CTA leaves, so only the time limit ends it (not the abort
+// flag).
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity,
+                                                uint64_t timeout_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63u) == 0u && globaltimer_ns() - t0 > timeout_ns) return false;
+    }
+}
+
 // ---------------------------------------------------------------------------
 // TMA (cp.async.bulk.tensor), tile mode, completion on an mbarrier
 // ---------------------------------------------------------------------------

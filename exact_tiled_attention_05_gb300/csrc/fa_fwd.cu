@@ -4,15 +4,17 @@
 // share every K/V tile it streams ("FlashAttention 1–4" §"FlashAttention-2":
 // a thread block per query block, K/V streamed in the inner loop; two Q tiles
 // per CTA as in §"FlashAttention-4").  Roles, by warp:
-//   warp 0      TMA producer: Q tiles once, then K_j, V_j into a ring of
-//               shared-memory stages guarded by full/empty mbarriers.
-//   warp 1      MMA issuer: S_t = Q_t K_j^T and O_t += P_t V_j on the tcgen05
-//               tensor cores, accumulators in tensor memory (TMEM).
-//   warp 2      allocates / frees TMEM.
-//   warps 4-7   softmax for Q tile 0, warps 8-11 for Q tile 1: one thread per
-//               query row reads its S row from TMEM, applies the causal/tail
-//               mask, runs the online-softmax update, writes P (bf16) back into
-//               TMEM over S, and at the end normalises O and writes O and lse.
+//   warp 0       TMA producer: Q tiles once, then K_j, V_j into a ring of
+//                shared-memory stages guarded by full/empty mbarriers.
+//   warp 1       MMA issuer (and TMEM allocation): S_t = Q_t K_j^T and
+//                O_t += P_t V_j on the tcgen05 tensor cores, accumulators in
+//                tensor memory (TMEM).
+//   warps 2-17   softmax, two threads per query row (16 warps: 2 tiles x 2
+//                column halves x 4 warps): each reads half of its S row from
+//                TMEM, applies the causal/tail mask, swaps the partial row max
+//                with its partner through shared memory, runs the online-softmax
+//                update, writes its half of P (bf16) back into TMEM over S, and
+//                at the end normalises its half of O and writes O and lse.
 //
 // Online softmax ("07 GPU、资源估算与 FlashAttention" §7.8; "CS336 Lecture 5
 // notes" §11.3-§11.4): per row a running max m (log2 units of the scaled
@@ -33,7 +35,9 @@ using namespace ptx;
 
 constexpr int kBM = 128;        // query rows per Q tile
 constexpr int kBN = 128;        // keys per K/V tile
-constexpr int kThreads = 384;   // 12 warps
+constexpr int kThreads = 576;   // 18 warps: TMA, MMA (+TMEM allocation), 2 tiles x 2 halves x 4 softmax
+constexpr int kFirstSoftmaxWarp = 2;
+constexpr int kSoftmaxPerTile = 256;  // threads per Q tile: two per query row
 constexpr int kBoxBytes = 128 * 64 * 2;  // one TMA box: 128 rows x 64 bf16
 // Conditional rescaling ("FlashAttention 1–4" §"FlashAttention-4"): the
 // reference max m only moves when a tile's max exceeds it by more than 8 (log2
@@ -65,9 +69,13 @@ struct alignas(1024) FwdSmem {
     uint64_t s_full[2];
     uint64_t p_full[2];
     uint64_t o_done[2];
+    uint64_t xchg[2];  // per tile: both halves of every row published their partial max
+    uint64_t xfin[2];  // per tile: both halves published their partial row sums
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
+    float xmax[2][2][2][128];  // [tile iteration parity][tile][half][row]
+    float xsum[2][2][2][128];  // [tile][half][fp32 sum, bf16 sum][row]
 };
 
 static_assert(sizeof(FwdSmem<128>) + 1024 <= 232448, "forward d=128 shared memory exceeds 227 KB");
@@ -135,13 +143,15 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(smem_u32(&sm.s_full[t]), 1);
-            mbar_init(smem_u32(&sm.p_full[t]), kBM);
+            mbar_init(smem_u32(&sm.p_full[t]), kSoftmaxPerTile);
+            mbar_init(smem_u32(&sm.xchg[t]), kSoftmaxPerTile);
+            mbar_init(smem_u32(&sm.xfin[t]), kSoftmaxPerTile);
             mbar_init(smem_u32(&sm.o_done[t]), 1);
         }
         mbar_init(smem_u32(&sm.drain), 1);
         fence_mbar_init();
     }
-    if (warp == 2) {
+    if (warp == 1) {
         tmem_alloc(smem_u32(&sm.tmem_base), Cfg::kTmemCols);
         tmem_relinquish();
     }
@@ -264,63 +274,72 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
             umma_commit(smem_u32(&sm.drain));
             mbar_wait_drain(smem_u32(&sm.drain), 0, kWaitTimeoutNs);
         }
-    } else if (warp >= 4) {
+    } else {
         // ===================== softmax / epilogue =====================
-        const int t = (warp - 4) >> 2;
-        const int wq = warp & 3;  // TMEM lane quarter this warp may access
+        // Two threads per query row: softmax warps 8t..8t+3 (counted from warp 2)
+        // take key columns 0-63 of S_t and O columns [0, d/2), warps 8t+4..8t+7
+        // columns 64-127 and O columns [d/2, d); a warp reaches TMEM lanes
+        // 32*(warp % 4) .. +31, and every group of four warps covers all 128.
+        // The halves swap partial row maxima through shared memory every tile
+        // and partial row sums once at the end.
+        const int sw = warp - kFirstSoftmaxWarp;
+        const int t = sw >> 3;           // Q tile
+        const int half = (sw >> 2) & 1;  // column half
+        const int wq = warp & 3;         // TMEM lane quarter this warp may access
         const int row = wq * 32 + lane;
         const int my_q0 = t == 0 ? q0[0] : q0[1];
         const int my_nkv = t == 0 ? nkv[0] : nkv[1];
         const int qi = my_q0 + row;
+        constexpr int kOH = HD / 2;  // O columns per thread
         const uint32_t lane_addr = tbase + (static_cast<uint32_t>(wq * 32) << 16);
-        const uint32_t s_addr = lane_addr + (static_cast<uint32_t>(t) * Cfg::kSColStride);
-        const uint32_t o_addr = lane_addr + Cfg::kOCol0 + t * HD;
+        const uint32_t s_addr = lane_addr + (static_cast<uint32_t>(t) * Cfg::kSColStride) + half * 64;
+        const uint32_t p_addr = lane_addr + (static_cast<uint32_t>(t) * Cfg::kSColStride) + half * 32;
+        const uint32_t o_addr = lane_addr + Cfg::kOCol0 + t * HD + half * kOH;
         const float sl2 = args.scale_log2;
-        float m_ref = -INFINITY;  // running max, log2 units
-        uint64_t l_pair = f2_pack(0.f, 0.f);   // sum of fp32 weights (for lse), two partial sums
-        uint64_t lr_pair = f2_pack(0.f, 0.f);  // sum of the bf16 weights (normalises O)
+        float m_ref = -INFINITY;               // running max, log2 units
+        uint64_t l_pair = f2_pack(0.f, 0.f);   // this half's sum of fp32 weights (for lse)
+        uint64_t lr_pair = f2_pack(0.f, 0.f);  // this half's sum of bf16 weights (normalises O)
         const uint64_t sl2_pair = f2_pack(sl2, sl2);
         bool ok = true;
         for (int j = 0; j < my_nkv; ++j) {
             ok = mbar_wait_warp(smem_u32(&sm.s_full[t]), j & 1, kWaitTimeoutNs, abort);
             if (!ok) break;
             tc_fence_after();
-            uint32_t sr[kBN];
-            {
-                uint32_t(&r0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[0]);
-                uint32_t(&r1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[32]);
-                uint32_t(&r2)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[64]);
-                uint32_t(&r3)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[96]);
-                tmem_ld32(s_addr + 0, r0);
-                tmem_ld32(s_addr + 32, r1);
-                tmem_ld32(s_addr + 64, r2);
-                tmem_ld32(s_addr + 96, r3);
-                tmem_wait_ld();
-                reg_fence(r0);
-                reg_fence(r1);
-                reg_fence(r2);
-                reg_fence(r3);
-            }
-            const int kbase = j * kBN;
-            const bool edge = (kbase + kBN > N) || (args.causal && kbase + kBN - 1 > my_q0);
+            uint32_t sa[32], sb[32];  // this half's 64 scores: columns [0,32) and [32,64)
+            tmem_ld32(s_addr + 0, sa);
+            tmem_ld32(s_addr + 32, sb);
+            tmem_wait_ld();
+            reg_fence(sa);
+            reg_fence(sb);
+#define SR(c) ((c) < 32 ? sa[(c)] : sb[(c) - 32])
+            const int kbase = j * kBN + half * 64;
+            const bool edge = (j * kBN + kBN > N) || (args.causal && j * kBN + kBN - 1 > my_q0);
             if (edge) {
                 const int kend = args.causal ? min(N, qi + 1) : N;
 #pragma unroll
-                for (int c = 0; c < kBN; ++c)
-                    if (kbase + c >= kend) sr[c] = __float_as_uint(-INFINITY);
+                for (int c = 0; c < 32; ++c) {
+                    if (kbase + c >= kend) sa[c] = __float_as_uint(-INFINITY);
+                    if (kbase + 32 + c >= kend) sb[c] = __float_as_uint(-INFINITY);
+                }
             }
-            // row max: four independent chains of 3-input max
+            // partial row max over this half: four chains of 3-input max
             float mc[4];
 #pragma unroll
-            for (int g = 0; g < 4; ++g) mc[g] = __uint_as_float(sr[g]);
+            for (int g = 0; g < 4; ++g) mc[g] = __uint_as_float(sa[g]);
 #pragma unroll
-            for (int c = 4; c < kBN; c += 8) {
+            for (int c = 4; c < 64; c += 8) {
 #pragma unroll
                 for (int g = 0; g < 4; ++g)
-                    mc[g] = fmax3(mc[g], __uint_as_float(sr[c + g]), __uint_as_float(sr[c + 4 + g]));
+                    mc[g] = fmax3(mc[g], __uint_as_float(SR(c + g)), __uint_as_float(SR(c + 4 + g)));
             }
-            const float mx2 = fmax3(mc[0], mc[1], fmaxf(mc[2], mc[3])) * sl2;
-            // running-max update; O and l are rescaled when the max rises
+            const float pm = fmax3(mc[0], mc[1], fmaxf(mc[2], mc[3]));
+            sm.xmax[j & 1][t][half][row] = pm;
+            mbar_arrive(smem_u32(&sm.xchg[t]));
+            ok = mbar_wait_warp(smem_u32(&sm.xchg[t]), j & 1, kWaitTimeoutNs, abort);
+            if (!ok) break;
+            const float mx2 = fmaxf(pm, sm.xmax[j & 1][t][half ^ 1][row]) * sl2;
+            // running-max update; O and the sums are rescaled when it rises by more
+            // than the threshold (both halves take the same decision)
             bool rescale = false;
             float alpha = 1.f;
             if (m_ref == -INFINITY) {
@@ -332,15 +351,37 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                 lr_pair = f2_mul(lr_pair, f2_pack(alpha, alpha));
                 m_ref = mx2;
             }
+            const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
+            const uint64_t negm_pair = f2_pack(neg_m, neg_m);
+            // P = exp2(s * scale * log2e - m) as packed bf16 pairs; both halves' S
+            // loads finished before the exchange, so P may overwrite S columns.
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int e = hh * 32 + 2 * i;
+                    const float2 x = f2_unpack(f2_fma(f2_pack_u(SR(e), SR(e + 1)), sl2_pair, negm_pair));
+                    const float p0 = ex2(x.x);
+                    const float p1 = ex2(x.y);
+                    l_pair = f2_add(l_pair, f2_pack(p0, p1));
+                    pk[i] = pack_bf16x2(p0, p1);
+                    lr_pair = f2_add(lr_pair, f2_pack_u(pk[i] << 16, pk[i] & 0xffff0000u));
+                }
+                tmem_st16(p_addr + hh * 16, pk);
+            }
+#undef SR
+            tmem_wait_st();
             if (__any_sync(0xffffffffu, rescale)) {
-                // O already holds P V of earlier tiles: wait for the latest one.
+                // O already holds P V of earlier tiles: wait for the latest one,
+                // then rescale it before this tile's P V is issued.
                 ok = mbar_wait_warp(smem_u32(&sm.o_done[t]), (j - 1) & 1, kWaitTimeoutNs, abort);
                 if (!ok) break;
                 tc_fence_after();
                 const uint64_t a2 = f2_pack(alpha, alpha);
-                uint32_t r[32];
-#pragma unroll 1
-                for (int c = 0; c < HD / 32; ++c) {
+#pragma unroll
+                for (int c = 0; c < kOH / 32; ++c) {
+                    uint32_t r[32];
                     tmem_ld32(o_addr + c * 32, r);
                     tmem_wait_ld();
                     reg_fence(r);
@@ -354,45 +395,30 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                 }
                 tmem_wait_st();
             }
-            const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
-            const uint64_t negm_pair = f2_pack(neg_m, neg_m);
-            // P = exp2(s * scale * log2e - m), packed bf16 pairs over S columns [0, 64)
-#pragma unroll
-            for (int c = 0; c < kBN / 32; ++c) {
-                uint32_t pk[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int e = c * 32 + 2 * i;
-                    const float2 x = f2_unpack(f2_fma(f2_pack_u(sr[e], sr[e + 1]), sl2_pair, negm_pair));
-                    const float p0 = ex2(x.x);
-                    const float p1 = ex2(x.y);
-                    l_pair = f2_add(l_pair, f2_pack(p0, p1));
-                    pk[i] = pack_bf16x2(p0, p1);
-                    lr_pair = f2_add(lr_pair, f2_pack_u(pk[i] << 16, pk[i] & 0xffff0000u));
-                }
-                tmem_st16(s_addr + c * 16, pk);
-            }
-            tmem_wait_st();
             tc_fence_before();
             mbar_arrive(smem_u32(&sm.p_full[t]));
         }
-        const float2 l_parts = f2_unpack(l_pair);
-        const float l_sum = l_parts.x + l_parts.y;
-        const float2 lr_parts = f2_unpack(lr_pair);
-        const float l_round = lr_parts.x + lr_parts.y;
         if (!ok) {
             if (lane == 0) record_timeout(args, abort);
         } else if (my_nkv > 0) {
-            ok = mbar_wait_warp(smem_u32(&sm.o_done[t]), (my_nkv - 1) & 1, kWaitTimeoutNs, abort);
+            const float2 lp = f2_unpack(l_pair);
+            const float2 lrp = f2_unpack(lr_pair);
+            sm.xsum[t][half][0][row] = lp.x + lp.y;
+            sm.xsum[t][half][1][row] = lrp.x + lrp.y;
+            mbar_arrive(smem_u32(&sm.xfin[t]));
+            ok = mbar_wait_warp(smem_u32(&sm.xfin[t]), 0, kWaitTimeoutNs, abort) &&
+                 mbar_wait_warp(smem_u32(&sm.o_done[t]), (my_nkv - 1) & 1, kWaitTimeoutNs, abort);
             if (ok) {
                 tc_fence_after();
+                const float l_sum = sm.xsum[t][0][0][row] + sm.xsum[t][1][0][row];
+                const float l_round = sm.xsum[t][0][1][row] + sm.xsum[t][1][1][row];
                 const float inv_l = 1.f / l_round;
                 const bool store = qi < N;
-                const size_t row_off = (static_cast<size_t>(bh) * N + qi) * HD;
+                const size_t row_off = (static_cast<size_t>(bh) * N + qi) * HD + half * kOH;
                 uint8_t* orow = reinterpret_cast<uint8_t*>(args.o) + row_off * 2;
-                uint32_t r[32];
-#pragma unroll 1
-                for (int c = 0; c < HD / 32; ++c) {
+#pragma unroll
+                for (int c = 0; c < kOH / 32; ++c) {
+                    uint32_t r[32];
                     tmem_ld32(o_addr + c * 32, r);
                     tmem_wait_ld();
                     reg_fence(r);
@@ -408,7 +434,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                                          pk[4 * v4 + 2], pk[4 * v4 + 3]);
                     }
                 }
-                if (store)
+                if (store && half == 0)
                     args.lse[static_cast<size_t>(bh) * N + qi] =
                         (m_ref + __log2f(l_sum)) * 0.69314718055994531f;
             } else if (lane == 0) {
@@ -419,7 +445,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 2) {
+    if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tbase, Cfg::kTmemCols);
     }

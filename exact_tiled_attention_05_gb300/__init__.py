@@ -210,3 +210,45 @@ def backward(q, k, v, o, lse, dout, scale=None, causal=False, dq=None, dk=None, 
 def sync_status(stream=None):
     """Synchronise the stream and raise if a kernel reported a device timeout."""
     _check(fa_sync_status(_stream_handle(stream)), "device status")
+
+
+# ---------------------------------------------------------------------------
+# autograd
+# ---------------------------------------------------------------------------
+
+def _make_function():
+    torch = _torch()
+
+    class _Attention(torch.autograd.Function):
+        """Exact attention with the fused forward and the recompute backward.
+        Saves q, k, v, o (bf16) and lse (fp32) for the backward."""
+
+        @staticmethod
+        def forward(ctx, q, k, v, scale, causal):
+            o, lse = forward(q, k, v, scale=scale, causal=causal)
+            ctx.save_for_backward(q, k, v, o, lse)
+            ctx.scale, ctx.causal = scale, causal
+            return o
+
+        @staticmethod
+        def backward(ctx, do):
+            q, k, v, o, lse = ctx.saved_tensors
+            dq, dk, dv = backward(q, k, v, o, lse, do.contiguous(), scale=ctx.scale,
+                                  causal=ctx.causal)
+            return dq, dk, dv, None, None
+
+    return _Attention
+
+
+_attention_fn = None
+
+
+def attention(q, k, v, scale=None, causal=False):
+    """Differentiable exact attention: O = softmax(scale q k^T [+ causal mask]) v.
+    q, k, v: contiguous bf16 CUDA tensors [B, H, N, d], d in {64, 128}."""
+    global _attention_fn
+    if _attention_fn is None:
+        _attention_fn = _make_function()
+    d = q.shape[-1]
+    s = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    return _attention_fn.apply(q, k, v, s, bool(causal))

@@ -49,6 +49,17 @@ constexpr int kBoxBytes = 128 * 64 * 2;  // one TMA box: 128 rows x 64 bf16
 // fp32 sum of the unrounded weights.
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
+// Software exp2 for a fraction of the elements ("FlashAttention 1–4"
+// §"FlashAttention-4"): with kSoftExpEvery = k > 0, every k-th pair of
+// exponentials in a row is computed on the FMA pipes instead of the exp unit.
+// Off by default: on GB300 each 128x128 softmax step is bound by instruction
+// issue on its SM sub-partition rather than by the exp unit, and every tested
+// fraction (1/4, 1/3, 1/2) measured slower.  Builds may set FA_SOFT_EXP_EVERY.
+#ifndef FA_SOFT_EXP_EVERY
+#define FA_SOFT_EXP_EVERY 0
+#endif
+constexpr int kSoftExpEvery = FA_SOFT_EXP_EVERY;
+
 template <int HD>
 struct FwdCfg {
     static constexpr int kTileBytes = kBN * HD * 2;
@@ -361,9 +372,19 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     const int e = hh * 32 + 2 * i;
-                    const float2 x = f2_unpack(f2_fma(f2_pack_u(SR(e), SR(e + 1)), sl2_pair, negm_pair));
-                    const float p0 = ex2(x.x);
-                    const float p1 = ex2(x.y);
+                    const uint64_t x2 = f2_fma(f2_pack_u(SR(e), SR(e + 1)), sl2_pair, negm_pair);
+                    float p0, p1;
+                    if (kSoftExpEvery > 0 && (i % (kSoftExpEvery > 0 ? kSoftExpEvery : 1)) ==
+                                                 kSoftExpEvery - 1) {
+                        // this pair on the FMA pipes, the rest on the exp unit
+                        const float2 pv = f2_unpack(exp2_fma_pair(x2));
+                        p0 = pv.x;
+                        p1 = pv.y;
+                    } else {
+                        const float2 x = f2_unpack(x2);
+                        p0 = ex2(x.x);
+                        p1 = ex2(x.y);
+                    }
                     l_pair = f2_add(l_pair, f2_pack(p0, p1));
                     pk[i] = pack_bf16x2(p0, p1);
                     lr_pair = f2_add(lr_pair, f2_pack_u(pk[i] << 16, pk[i] & 0xffff0000u));

@@ -397,6 +397,30 @@ __device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
     return r;
 }
 
+// 2^x for a pair of floats on the FMA pipes (no MUFU), relative error 1.2e-4.
+// Cody-Waite style split x = j + f with j = round(x), f in [-1/2, 1/2]: adding
+// 1.5 * 2^23 rounds x to an integer held in the low mantissa bits; 2^f is a
+// cubic fitted by relative-error-weighted least squares on Chebyshev nodes
+// (csrc/fit_exp2_poly.py prints these coefficients); 2^j is applied by adding
+// j to the exponent field.  Inputs below -125 (including -inf) are clamped, so
+// the result is >= 2^-125 and never denormal.
+__device__ __forceinline__ uint64_t exp2_fma_pair(uint64_t x2) {
+    const float2 xin = f2_unpack(x2);
+    const uint64_t x = f2_pack(fmaxf(xin.x, -125.f), fmaxf(xin.y, -125.f));
+    const float kMagic = 12582912.f;  // 1.5 * 2^23
+    const uint64_t magic = f2_pack(kMagic, kMagic);
+    const uint64_t t = f2_add(x, magic);
+    const uint64_t f = f2_sub(x, f2_sub(t, magic));
+    uint64_t p = f2_fma(f2_pack(0.054592825f, 0.054592825f), f, f2_pack(0.24221784f, 0.24221784f));
+    p = f2_fma(p, f, f2_pack(0.6933686f, 0.6933686f));
+    p = f2_fma(p, f, f2_pack(1.0f, 1.0f));
+    const float2 tt = f2_unpack(t), pp = f2_unpack(p);
+    const int kMagicBits = 0x4B400000;  // bit pattern of 1.5 * 2^23
+    const float r0 = __int_as_float(__float_as_int(pp.x) + ((__float_as_int(tt.x) - kMagicBits) << 23));
+    const float r1 = __int_as_float(__float_as_int(pp.y) + ((__float_as_int(tt.y) - kMagicBits) << 23));
+    return f2_pack(r0, r1);
+}
+
 // max(a, b, c) in one instruction.
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float r;

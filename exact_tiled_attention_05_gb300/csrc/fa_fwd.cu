@@ -86,7 +86,7 @@ struct alignas(1024) FwdSmem {
     uint32_t tmem_base;
     int abort;
     float xmax[2][2][2][128];  // [tile iteration parity][tile][half][row]
-    float xsum[2][2][2][128];  // [tile][half][fp32 sum, bf16 sum][row]
+    float xsum[2][2][2][128];  // [tile][half][fp32 sum, rounding correction][row]
 };
 
 static_assert(sizeof(FwdSmem<128>) + 1024 <= 232448, "forward d=128 shared memory exceeds 227 KB");
@@ -309,7 +309,10 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
         const float sl2 = args.scale_log2;
         float m_ref = -INFINITY;               // running max, log2 units
         uint64_t l_pair = f2_pack(0.f, 0.f);   // this half's sum of fp32 weights (for lse)
-        uint64_t lr_pair = f2_pack(0.f, 0.f);  // this half's sum of bf16 weights (normalises O)
+        // Correction that turns l into the sum of the bf16 weights P V actually used,
+        // for the largest weight of each half-tile only: that weight's rounding is
+        // what biases O when one key dominates, the others' errors average out.
+        float lc = 0.f;
         const uint64_t sl2_pair = f2_pack(sl2, sl2);
         bool ok = true;
         for (int j = 0; j < my_nkv; ++j) {
@@ -359,7 +362,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                 rescale = true;
                 alpha = ex2(m_ref - mx2);
                 l_pair = f2_mul(l_pair, f2_pack(alpha, alpha));
-                lr_pair = f2_mul(lr_pair, f2_pack(alpha, alpha));
+                lc *= alpha;
                 m_ref = mx2;
             }
             const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
@@ -387,11 +390,15 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                     }
                     l_pair = f2_add(l_pair, f2_pack(p0, p1));
                     pk[i] = pack_bf16x2(p0, p1);
-                    lr_pair = f2_add(lr_pair, f2_pack_u(pk[i] << 16, pk[i] & 0xffff0000u));
                 }
                 tmem_st16(p_addr + hh * 16, pk);
             }
 #undef SR
+            {
+                // the loop's rounding steps applied to this half's largest score
+                const float pmx = ex2(fmaf(pm, sl2, neg_m));
+                lc += __uint_as_float(pack_bf16x2(pmx, 0.f) << 16) - pmx;
+            }
             tmem_wait_st();
             if (__any_sync(0xffffffffu, rescale)) {
                 // O already holds P V of earlier tiles: wait for the latest one,
@@ -423,16 +430,15 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
             if (lane == 0) record_timeout(args, abort);
         } else if (my_nkv > 0) {
             const float2 lp = f2_unpack(l_pair);
-            const float2 lrp = f2_unpack(lr_pair);
             sm.xsum[t][half][0][row] = lp.x + lp.y;
-            sm.xsum[t][half][1][row] = lrp.x + lrp.y;
+            sm.xsum[t][half][1][row] = lc;
             mbar_arrive(smem_u32(&sm.xfin[t]));
             ok = mbar_wait_warp(smem_u32(&sm.xfin[t]), 0, kWaitTimeoutNs, abort) &&
                  mbar_wait_warp(smem_u32(&sm.o_done[t]), (my_nkv - 1) & 1, kWaitTimeoutNs, abort);
             if (ok) {
                 tc_fence_after();
                 const float l_sum = sm.xsum[t][0][0][row] + sm.xsum[t][1][0][row];
-                const float l_round = sm.xsum[t][0][1][row] + sm.xsum[t][1][1][row];
+                const float l_round = l_sum + (sm.xsum[t][0][1][row] + sm.xsum[t][1][1][row]);
                 const float inv_l = 1.f / l_round;
                 const bool store = qi < N;
                 const size_t row_off = (static_cast<size_t>(bh) * N + qi) * HD + half * kOH;

@@ -52,9 +52,10 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 // Software exp2 for a fraction of the elements ("FlashAttention 1–4"
 // §"FlashAttention-4"): with kSoftExpEvery = k > 0, every k-th pair of
 // exponentials in a row is computed on the FMA pipes instead of the exp unit.
-// Off by default: on GB300 each 128x128 softmax step is bound by instruction
-// issue on its SM sub-partition rather than by the exp unit, and every tested
-// fraction (1/4, 1/3, 1/2) measured slower.  Builds may set FA_SOFT_EXP_EVERY.
+// Off by default: GB300's exp unit sustains about 32 exponentials per clock per
+// SM, twice what the tensor cores consume at d = 128, and each softmax step is
+// latency-bound, so every tested fraction (1/4, 1/3, 1/2) measured slower.
+// Builds may set FA_SOFT_EXP_EVERY.
 #ifndef FA_SOFT_EXP_EVERY
 #define FA_SOFT_EXP_EVERY 0
 #endif

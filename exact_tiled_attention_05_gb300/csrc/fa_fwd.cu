@@ -79,7 +79,7 @@ struct alignas(1024) FwdSmem {
     uint64_t kv_full[FwdCfg<HD>::kStages];
     uint64_t kv_empty[FwdCfg<HD>::kStages];
     uint64_t s_full[2];
-    uint64_t p_full[2];
+    uint64_t p_full[2][2];  // [tile][part]: P columns 0-15 and 32-47, then 16-31 and 48-63
     uint64_t o_done[2];
     uint64_t xchg[2];  // per tile: both halves of every row published their partial max
     uint64_t xfin[2];  // per tile: both halves published their partial row sums
@@ -155,7 +155,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(smem_u32(&sm.s_full[t]), 1);
-            mbar_init(smem_u32(&sm.p_full[t]), kSoftmaxPerTile);
+            mbar_init(smem_u32(&sm.p_full[t][0]), kSoftmaxPerTile);
+            mbar_init(smem_u32(&sm.p_full[t][1]), kSoftmaxPerTile);
             mbar_init(smem_u32(&sm.xchg[t]), kSoftmaxPerTile);
             mbar_init(smem_u32(&sm.xfin[t]), kSoftmaxPerTile);
             mbar_init(smem_u32(&sm.o_done[t]), 1);
@@ -232,13 +233,16 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                             sdesc_sw128(k_addr + off, 16, 1024), idesc_s, kk > 0);
                 }
             };
-            // O_t += P_t V : P (bf16) from TMEM, V MN-major, kBN/16 k-steps.
-            auto issue_pv = [&](int t, uint32_t v_addr, bool acc) {
+            // O_t += P_t V : P (bf16) from TMEM, V MN-major, in two parts of four
+            // k-steps of 16 keys: part 0 takes keys 0-31 and 64-95 (the first P
+            // columns each softmax thread stores), part 1 the rest.
+            auto issue_pv = [&](int t, uint32_t v_addr, int part, bool acc) {
 #pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk) {
+                for (int i = 0; i < 4; ++i) {
+                    const int kk = (i >> 1) * 4 + part * 2 + (i & 1);
                     umma_ts(tbase + Cfg::kOCol0 + t * HD, tbase + (static_cast<uint32_t>(t) * Cfg::kSColStride) + kk * 8,
                             sdesc_sw128(v_addr + kk * 16 * 128, kBoxBytes, 1024), idesc_o,
-                            (acc || kk > 0) ? 1u : 0u);
+                            (acc || part > 0 || i > 0) ? 1u : 0u);
                 }
             };
             if (ok && nmax > 0) {
@@ -260,10 +264,14 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                 bool k_ready = false;
                 for (int t = 0; t < 2 && ok; ++t) {
                     if (j < nkv[t]) {
-                        if (!(ok = mbar_wait(smem_u32(&sm.p_full[t]), j & 1, kWaitTimeoutNs, abort)))
-                            break;
-                        tc_fence_after();
-                        issue_pv(t, kv_addr(iv), j > 0);
+                        for (int part = 0; part < 2 && ok; ++part) {
+                            if (!(ok = mbar_wait(smem_u32(&sm.p_full[t][part]), j & 1, kWaitTimeoutNs,
+                                                 abort)))
+                                break;
+                            tc_fence_after();
+                            issue_pv(t, kv_addr(iv), part, j > 0);
+                        }
+                        if (!ok) break;
                         umma_commit(smem_u32(&sm.o_done[t]));
                     }
                     if (t == 1) umma_commit(smem_u32(&sm.kv_empty[iv % Cfg::kStages]));
@@ -370,6 +378,9 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
             const uint64_t negm_pair = f2_pack(neg_m, neg_m);
             // P = exp2(s * scale * log2e - m) as packed bf16 pairs; both halves' S
             // loads finished before the exchange, so P may overwrite S columns.
+            // Each thread stores its first 32 weights and signals part 0, so the
+            // MMA warp can start that part of P V while the rest are computed.
+            const bool any_rescale = __any_sync(0xffffffffu, rescale);
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
                 uint32_t pk[16];
@@ -393,39 +404,39 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                     pk[i] = pack_bf16x2(p0, p1);
                 }
                 tmem_st16(p_addr + hh * 16, pk);
+                if (hh == 0 && any_rescale) {
+                    // O already holds P V of earlier tiles: wait for the latest one,
+                    // then rescale it before any of this tile's P V is issued.
+                    ok = mbar_wait_warp(smem_u32(&sm.o_done[t]), (j - 1) & 1, kWaitTimeoutNs, abort);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint64_t a2 = f2_pack(alpha, alpha);
+#pragma unroll
+                    for (int c = 0; c < kOH / 16; ++c) {
+                        uint32_t r[16];
+                        tmem_ld16(o_addr + c * 16, r);
+                        tmem_wait_ld();
+                        reg_fence(r);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const float2 v = f2_unpack(f2_mul(f2_pack_u(r[2 * i], r[2 * i + 1]), a2));
+                            r[2 * i] = __float_as_uint(v.x);
+                            r[2 * i + 1] = __float_as_uint(v.y);
+                        }
+                        tmem_st16(o_addr + c * 16, r);
+                    }
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(smem_u32(&sm.p_full[t][hh]));
             }
 #undef SR
+            if (!ok) break;
             {
                 // the loop's rounding steps applied to this half's largest score
                 const float pmx = ex2(fmaf(pm, sl2, neg_m));
                 lc += __uint_as_float(pack_bf16x2(pmx, 0.f) << 16) - pmx;
             }
-            tmem_wait_st();
-            if (__any_sync(0xffffffffu, rescale)) {
-                // O already holds P V of earlier tiles: wait for the latest one,
-                // then rescale it before this tile's P V is issued.
-                ok = mbar_wait_warp(smem_u32(&sm.o_done[t]), (j - 1) & 1, kWaitTimeoutNs, abort);
-                if (!ok) break;
-                tc_fence_after();
-                const uint64_t a2 = f2_pack(alpha, alpha);
-#pragma unroll
-                for (int c = 0; c < kOH / 32; ++c) {
-                    uint32_t r[32];
-                    tmem_ld32(o_addr + c * 32, r);
-                    tmem_wait_ld();
-                    reg_fence(r);
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const float2 v = f2_unpack(f2_mul(f2_pack_u(r[2 * i], r[2 * i + 1]), a2));
-                        r[2 * i] = __float_as_uint(v.x);
-                        r[2 * i + 1] = __float_as_uint(v.y);
-                    }
-                    tmem_st32(o_addr + c * 32, r);
-                }
-                tmem_wait_st();
-            }
-            tc_fence_before();
-            mbar_arrive(smem_u32(&sm.p_full[t]));
         }
         if (!ok) {
             if (lane == 0) record_timeout(args, abort);

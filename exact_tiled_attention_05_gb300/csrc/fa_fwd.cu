@@ -61,6 +61,35 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 #endif
 constexpr int kSoftExpEvery = FA_SOFT_EXP_EVERY;
 
+// P is handed to the MMA warp in kPParts parts: each softmax thread stores
+// 32 / kPParts packed pairs of weights, then signals that part, so P V on the
+// first parts overlaps the exponentials of the later ones.
+#ifndef FA_P_PARTS
+#define FA_P_PARTS 2
+#endif
+constexpr int kPParts = FA_P_PARTS;
+static_assert(kPParts == 1 || kPParts == 2 || kPParts == 4, "P is signalled in 1, 2 or 4 parts");
+constexpr int kPairsPerPart = 32 / kPParts;
+
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* r) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+        : "memory");
+}
+
+// Stores N consecutive 32-bit TMEM columns of this thread's lane.
+template <int N>
+__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t* r) {
+    if constexpr (N == 8) {
+        tmem_st8(taddr, r);
+    } else {
+#pragma unroll
+        for (int c = 0; c < N; c += 16)
+            tmem_st16(taddr + c, *reinterpret_cast<const uint32_t(*)[16]>(r + c));
+    }
+}
+
 template <int HD>
 struct FwdCfg {
     static constexpr int kTileBytes = kBN * HD * 2;
@@ -79,7 +108,7 @@ struct alignas(1024) FwdSmem {
     uint64_t kv_full[FwdCfg<HD>::kStages];
     uint64_t kv_empty[FwdCfg<HD>::kStages];
     uint64_t s_full[2];
-    uint64_t p_full[2][2];  // [tile][part]: P columns 0-15 and 32-47, then 16-31 and 48-63
+    uint64_t p_full[2][kPParts];  // [tile][part of P]
     uint64_t o_done[2];
     uint64_t xchg[2];  // per tile: both halves of every row published their partial max
     uint64_t xfin[2];  // per tile: both halves published their partial row sums
@@ -155,8 +184,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(smem_u32(&sm.s_full[t]), 1);
-            mbar_init(smem_u32(&sm.p_full[t][0]), kSoftmaxPerTile);
-            mbar_init(smem_u32(&sm.p_full[t][1]), kSoftmaxPerTile);
+            for (int part = 0; part < kPParts; ++part)
+                mbar_init(smem_u32(&sm.p_full[t][part]), kSoftmaxPerTile);
             mbar_init(smem_u32(&sm.xchg[t]), kSoftmaxPerTile);
             mbar_init(smem_u32(&sm.xfin[t]), kSoftmaxPerTile);
             mbar_init(smem_u32(&sm.o_done[t]), 1);
@@ -233,13 +262,14 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                             sdesc_sw128(k_addr + off, 16, 1024), idesc_s, kk > 0);
                 }
             };
-            // O_t += P_t V : P (bf16) from TMEM, V MN-major, in two parts of four
-            // k-steps of 16 keys: part 0 takes keys 0-31 and 64-95 (the first P
-            // columns each softmax thread stores), part 1 the rest.
+            // O_t += P_t V : P (bf16) from TMEM, V MN-major, k-steps of 16 keys.
+            // Part q of P holds, from each of a row's two softmax threads, keys
+            // 64h + 32q/kPParts + [0, 32/kPParts): k-steps 4h + q*4/kPParts + i.
             auto issue_pv = [&](int t, uint32_t v_addr, int part, bool acc) {
+                constexpr int kSteps = 4 / kPParts;  // per half-row
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int kk = (i >> 1) * 4 + part * 2 + (i & 1);
+                for (int i = 0; i < 2 * kSteps; ++i) {
+                    const int kk = (i / kSteps) * 4 + part * kSteps + (i % kSteps);
                     umma_ts(tbase + Cfg::kOCol0 + t * HD, tbase + (static_cast<uint32_t>(t) * Cfg::kSColStride) + kk * 8,
                             sdesc_sw128(v_addr + kk * 16 * 128, kBoxBytes, 1024), idesc_o,
                             (acc || part > 0 || i > 0) ? 1u : 0u);
@@ -264,7 +294,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                 bool k_ready = false;
                 for (int t = 0; t < 2 && ok; ++t) {
                     if (j < nkv[t]) {
-                        for (int part = 0; part < 2 && ok; ++part) {
+                        for (int part = 0; part < kPParts && ok; ++part) {
                             if (!(ok = mbar_wait(smem_u32(&sm.p_full[t][part]), j & 1, kWaitTimeoutNs,
                                                  abort)))
                                 break;
@@ -378,15 +408,15 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
             const uint64_t negm_pair = f2_pack(neg_m, neg_m);
             // P = exp2(s * scale * log2e - m) as packed bf16 pairs; both halves' S
             // loads finished before the exchange, so P may overwrite S columns.
-            // Each thread stores its first 32 weights and signals part 0, so the
-            // MMA warp can start that part of P V while the rest are computed.
+            // Each part of P is signalled as soon as it is stored, so the MMA warp
+            // starts P V on it while the later parts are computed.
             const bool any_rescale = __any_sync(0xffffffffu, rescale);
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                uint32_t pk[16];
+            for (int hh = 0; hh < kPParts; ++hh) {
+                uint32_t pk[kPairsPerPart];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int e = hh * 32 + 2 * i;
+                for (int i = 0; i < kPairsPerPart; ++i) {
+                    const int e = hh * 2 * kPairsPerPart + 2 * i;
                     const uint64_t x2 = f2_fma(f2_pack_u(SR(e), SR(e + 1)), sl2_pair, negm_pair);
                     float p0, p1;
                     if (kSoftExpEvery > 0 && (i % (kSoftExpEvery > 0 ? kSoftExpEvery : 1)) ==
@@ -403,7 +433,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                     l_pair = f2_add(l_pair, f2_pack(p0, p1));
                     pk[i] = pack_bf16x2(p0, p1);
                 }
-                tmem_st16(p_addr + hh * 16, pk);
+                tmem_st_cols<kPairsPerPart>(p_addr + hh * kPairsPerPart, pk);
                 if (hh == 0 && any_rescale) {
                     // O already holds P V of earlier tiles: wait for the latest one,
                     // then rescale it before any of this tile's P V is issued.

@@ -61,33 +61,56 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 #endif
 constexpr int kSoftExpEvery = FA_SOFT_EXP_EVERY;
 
-// P is handed to the MMA warp in kPParts parts: each softmax thread stores
-// 32 / kPParts packed pairs of weights, then signals that part, so P V on the
-// first parts overlaps the exponentials of the later ones.
-#ifndef FA_P_PARTS
-#define FA_P_PARTS 2
-#endif
-constexpr int kPParts = FA_P_PARTS;
-static_assert(kPParts == 1 || kPParts == 2 || kPParts == 4, "P is signalled in 1, 2 or 4 parts");
-constexpr int kPairsPerPart = 32 / kPParts;
+// P is handed to the MMA warp in two parts, keys 0-63 and 64-127 of the tile:
+// P V on the first part overlaps the exponentials of the second.
+constexpr int kPParts = 2;
 
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* r) {
+// TMEM accesses of 16 lanes: lane L of the warp holds rows L/4 and L/4 + 8 of
+// the 16 addressed.  16x256b: per repetition i, registers 4i..4i+3 are columns
+// 8i + 2(L%4) + {0, 1} of the first row, then the same of the second.
+// 16x128b: per repetition i, registers 2i, 2i+1 are column 4i + L%4 of the
+// first and of the second row.
+__device__ __forceinline__ void tmem_ld_16x256b_x8(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+        "tcgen05.ld.sync.aligned.16x256b.x8.b32"
+        " {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15,"
+        " %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld_16x256b_x4(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x4.b32"
+        " {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st_16x256b_x4(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.16x256b.x4.b32"
+        " [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(
+            taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
         : "memory");
 }
 
-// Stores N consecutive 32-bit TMEM columns of this thread's lane.
-template <int N>
-__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t* r) {
-    if constexpr (N == 8) {
-        tmem_st8(taddr, r);
-    } else {
-#pragma unroll
-        for (int c = 0; c < N; c += 16)
-            tmem_st16(taddr + c, *reinterpret_cast<const uint32_t(*)[16]>(r + c));
-    }
+__device__ __forceinline__ void tmem_st_16x128b_x8(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.16x128b.x8.b32"
+        " [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(
+            taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
 }
 
 template <int HD>
@@ -110,13 +133,9 @@ struct alignas(1024) FwdSmem {
     uint64_t s_full[2];
     uint64_t p_full[2][kPParts];  // [tile][part of P]
     uint64_t o_done[2];
-    uint64_t xchg[2];  // per tile: both halves of every row published their partial max
-    uint64_t xfin[2];  // per tile: both halves published their partial row sums
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
-    float xmax[2][2][2][128];  // [tile iteration parity][tile][half][row]
-    float xsum[2][2][2][128];  // [tile][half][fp32 sum, rounding correction][row]
 };
 
 static_assert(sizeof(FwdSmem<128>) + 1024 <= 232448, "forward d=128 shared memory exceeds 227 KB");
@@ -186,8 +205,6 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
             mbar_init(smem_u32(&sm.s_full[t]), 1);
             for (int part = 0; part < kPParts; ++part)
                 mbar_init(smem_u32(&sm.p_full[t][part]), kSoftmaxPerTile);
-            mbar_init(smem_u32(&sm.xchg[t]), kSoftmaxPerTile);
-            mbar_init(smem_u32(&sm.xfin[t]), kSoftmaxPerTile);
             mbar_init(smem_u32(&sm.o_done[t]), 1);
         }
         mbar_init(smem_u32(&sm.drain), 1);
@@ -262,14 +279,12 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                             sdesc_sw128(k_addr + off, 16, 1024), idesc_s, kk > 0);
                 }
             };
-            // O_t += P_t V : P (bf16) from TMEM, V MN-major, k-steps of 16 keys.
-            // Part q of P holds, from each of a row's two softmax threads, keys
-            // 64h + 32q/kPParts + [0, 32/kPParts): k-steps 4h + q*4/kPParts + i.
+            // O_t += P_t V : P (bf16) from TMEM, V MN-major, k-steps of 16 keys;
+            // part q of P (keys 64q..64q+63) is k-steps 4q..4q+3.
             auto issue_pv = [&](int t, uint32_t v_addr, int part, bool acc) {
-                constexpr int kSteps = 4 / kPParts;  // per half-row
 #pragma unroll
-                for (int i = 0; i < 2 * kSteps; ++i) {
-                    const int kk = (i / kSteps) * 4 + part * kSteps + (i % kSteps);
+                for (int i = 0; i < 4; ++i) {
+                    const int kk = part * 4 + i;
                     umma_ts(tbase + Cfg::kOCol0 + t * HD, tbase + (static_cast<uint32_t>(t) * Cfg::kSColStride) + kk * 8,
                             sdesc_sw128(v_addr + kk * 16 * 128, kBoxBytes, 1024), idesc_o,
                             (acc || part > 0 || i > 0) ? 1u : 0u);
@@ -326,134 +341,174 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
         }
     } else {
         // ===================== softmax / epilogue =====================
-        // Two threads per query row: softmax warps 8t..8t+3 (counted from warp 2)
-        // take key columns 0-63 of S_t and O columns [0, d/2), warps 8t+4..8t+7
-        // columns 64-127 and O columns [d/2, d); a warp reaches TMEM lanes
-        // 32*(warp % 4) .. +31, and every group of four warps covers all 128.
-        // The halves swap partial row maxima through shared memory every tile
-        // and partial row sums once at the end.
+        // Softmax warps 8t..8t+7 (counted from warp 2) own Q tile t.  Warp
+        // (wq, sub), wq = warp % 4 the TMEM lane quarter it may access and sub
+        // which 16 of those 32 lanes, reads S_t with the 16x256b shape: lane L
+        // holds rows rA = 32 wq + 16 sub + L/4 and rB = rA + 8, key columns
+        // 8i + 2(L%4) + {0, 1}, i = 0..15.  The four threads of a row sit in one
+        // warp, so row maxima and sums are combined with two shuffles, and every
+        // reader of a row's S columns has passed tcgen05.wait::ld before the warp
+        // overwrites them with P.
         const int sw = warp - kFirstSoftmaxWarp;
-        const int t = sw >> 3;           // Q tile
-        const int half = (sw >> 2) & 1;  // column half
-        const int wq = warp & 3;         // TMEM lane quarter this warp may access
-        const int row = wq * 32 + lane;
+        const int t = sw >> 3;          // Q tile
+        const int sub = (sw >> 2) & 1;  // lanes 0-15 or 16-31 of the quarter
+        const int wq = warp & 3;        // TMEM lane quarter this warp may access
+        const int cq = lane & 3;        // column group within the row's four threads
+        const int rA = wq * 32 + sub * 16 + (lane >> 2);
         const int my_q0 = t == 0 ? q0[0] : q0[1];
         const int my_nkv = t == 0 ? nkv[0] : nkv[1];
-        const int qi = my_q0 + row;
-        constexpr int kOH = HD / 2;  // O columns per thread
-        const uint32_t lane_addr = tbase + (static_cast<uint32_t>(wq * 32) << 16);
-        const uint32_t s_addr = lane_addr + (static_cast<uint32_t>(t) * Cfg::kSColStride) + half * 64;
-        const uint32_t p_addr = lane_addr + (static_cast<uint32_t>(t) * Cfg::kSColStride) + half * 32;
-        const uint32_t o_addr = lane_addr + Cfg::kOCol0 + t * HD + half * kOH;
+        const int qA = my_q0 + rA, qB = qA + 8;
+        const uint32_t lanes16 = tbase + (static_cast<uint32_t>(wq * 32 + sub * 16) << 16);
+        const uint32_t s_addr = lanes16 + static_cast<uint32_t>(t) * Cfg::kSColStride;
+        const uint32_t o_addr = lanes16 + Cfg::kOCol0 + t * HD;
         const float sl2 = args.scale_log2;
-        float m_ref = -INFINITY;               // running max, log2 units
-        uint64_t l_pair = f2_pack(0.f, 0.f);   // this half's sum of fp32 weights (for lse)
-        // Correction that turns l into the sum of the bf16 weights P V actually used,
-        // for the largest weight of each half-tile only: that weight's rounding is
-        // what biases O when one key dominates, the others' errors average out.
-        float lc = 0.f;
+        // Per row (A, B): running max in log2 units, this thread's share of the
+        // fp32 row sum (for lse), and a correction that turns the row sum into the
+        // sum of the bf16 weights P V actually used, for the largest weight of each
+        // tile only: that weight's rounding is what biases O when one key
+        // dominates, the other weights' rounding errors average out.
+        float mA = -INFINITY, mB = -INFINITY;
+        uint64_t lA = f2_pack(0.f, 0.f), lB = f2_pack(0.f, 0.f);
+        float lcA = 0.f, lcB = 0.f;
         const uint64_t sl2_pair = f2_pack(sl2, sl2);
         bool ok = true;
         for (int j = 0; j < my_nkv; ++j) {
             ok = mbar_wait_warp(smem_u32(&sm.s_full[t]), j & 1, kWaitTimeoutNs, abort);
             if (!ok) break;
             tc_fence_after();
-            uint32_t sa[32], sb[32];  // this half's 64 scores: columns [0,32) and [32,64)
-            tmem_ld32(s_addr + 0, sa);
-            tmem_ld32(s_addr + 32, sb);
+            uint32_t sa[32], sb[32];  // keys 0-63 and 64-127 of the tile
+            tmem_ld_16x256b_x8(s_addr, sa);
+            tmem_ld_16x256b_x8(s_addr + 64, sb);
             tmem_wait_ld();
             reg_fence(sa);
             reg_fence(sb);
+            // register e of the part: repetition e/4, row A for e%4 < 2, key 8(e/4) + 2cq + e%2
 #define SR(c) ((c) < 32 ? sa[(c)] : sb[(c) - 32])
-            const int kbase = j * kBN + half * 64;
+            const int kbase = j * kBN + 2 * cq;
             const bool edge = (j * kBN + kBN > N) || (args.causal && j * kBN + kBN - 1 > my_q0);
             if (edge) {
-                const int kend = args.causal ? min(N, qi + 1) : N;
+                const int kendA = args.causal ? min(N, qA + 1) : N;
+                const int kendB = args.causal ? min(N, qB + 1) : N;
 #pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    if (kbase + c >= kend) sa[c] = __float_as_uint(-INFINITY);
-                    if (kbase + 32 + c >= kend) sb[c] = __float_as_uint(-INFINITY);
+                for (int i = 0; i < 8; ++i) {
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        const int ka = kbase + 8 * i + c, kb = ka + 64;
+                        if (ka >= kendA) sa[4 * i + c] = __float_as_uint(-INFINITY);
+                        if (ka >= kendB) sa[4 * i + 2 + c] = __float_as_uint(-INFINITY);
+                        if (kb >= kendA) sb[4 * i + c] = __float_as_uint(-INFINITY);
+                        if (kb >= kendB) sb[4 * i + 2 + c] = __float_as_uint(-INFINITY);
+                    }
                 }
             }
-            // partial row max over this half: four chains of 3-input max
-            float mc[4];
+            // row maxima: 32 values per row in this thread, then across the four
+            float ma[2], mb[2];
+            ma[0] = __uint_as_float(sa[0]);
+            ma[1] = __uint_as_float(sa[1]);
+            mb[0] = __uint_as_float(sa[2]);
+            mb[1] = __uint_as_float(sa[3]);
 #pragma unroll
-            for (int g = 0; g < 4; ++g) mc[g] = __uint_as_float(sa[g]);
+            for (int i = 1; i < 15; i += 2) {  // repetitions 1..14 in pairs
 #pragma unroll
-            for (int c = 4; c < 64; c += 8) {
-#pragma unroll
-                for (int g = 0; g < 4; ++g)
-                    mc[g] = fmax3(mc[g], __uint_as_float(SR(c + g)), __uint_as_float(SR(c + 4 + g)));
+                for (int c = 0; c < 2; ++c) {
+                    ma[c] = fmax3(ma[c], __uint_as_float(SR(4 * i + c)),
+                                  __uint_as_float(SR(4 * i + 4 + c)));
+                    mb[c] = fmax3(mb[c], __uint_as_float(SR(4 * i + 2 + c)),
+                                  __uint_as_float(SR(4 * i + 6 + c)));
+                }
             }
-            const float pm = fmax3(mc[0], mc[1], fmaxf(mc[2], mc[3]));
-            sm.xmax[j & 1][t][half][row] = pm;
-            mbar_arrive(smem_u32(&sm.xchg[t]));
-            ok = mbar_wait_warp(smem_u32(&sm.xchg[t]), j & 1, kWaitTimeoutNs, abort);
-            if (!ok) break;
-            const float mx2 = fmaxf(pm, sm.xmax[j & 1][t][half ^ 1][row]) * sl2;
+            // repetition 15
+            float pmA = fmax3(ma[0], ma[1], fmaxf(__uint_as_float(sb[28]), __uint_as_float(sb[29])));
+            float pmB = fmax3(mb[0], mb[1], fmaxf(__uint_as_float(sb[30]), __uint_as_float(sb[31])));
+            pmA = fmaxf(pmA, __shfl_xor_sync(0xffffffffu, pmA, 1));
+            pmB = fmaxf(pmB, __shfl_xor_sync(0xffffffffu, pmB, 1));
+            pmA = fmaxf(pmA, __shfl_xor_sync(0xffffffffu, pmA, 2));
+            pmB = fmaxf(pmB, __shfl_xor_sync(0xffffffffu, pmB, 2));
             // running-max update; O and the sums are rescaled when it rises by more
-            // than the threshold (both halves take the same decision)
+            // than the threshold (the row's four threads take the same decision)
             bool rescale = false;
-            float alpha = 1.f;
-            if (m_ref == -INFINITY) {
-                m_ref = mx2;
-            } else if (mx2 > m_ref + kRescaleThreshold) {
-                rescale = true;
-                alpha = ex2(m_ref - mx2);
-                l_pair = f2_mul(l_pair, f2_pack(alpha, alpha));
-                lc *= alpha;
-                m_ref = mx2;
+            float alphaA = 1.f, alphaB = 1.f;
+            {
+                const float mxA = pmA * sl2, mxB = pmB * sl2;
+                if (mA == -INFINITY) {
+                    mA = mxA;
+                } else if (mxA > mA + kRescaleThreshold) {
+                    rescale = true;
+                    alphaA = ex2(mA - mxA);
+                    lA = f2_mul(lA, f2_pack(alphaA, alphaA));
+                    lcA *= alphaA;
+                    mA = mxA;
+                }
+                if (mB == -INFINITY) {
+                    mB = mxB;
+                } else if (mxB > mB + kRescaleThreshold) {
+                    rescale = true;
+                    alphaB = ex2(mB - mxB);
+                    lB = f2_mul(lB, f2_pack(alphaB, alphaB));
+                    lcB *= alphaB;
+                    mB = mxB;
+                }
             }
-            const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
-            const uint64_t negm_pair = f2_pack(neg_m, neg_m);
-            // P = exp2(s * scale * log2e - m) as packed bf16 pairs; both halves' S
-            // loads finished before the exchange, so P may overwrite S columns.
-            // Each part of P is signalled as soon as it is stored, so the MMA warp
-            // starts P V on it while the later parts are computed.
+            const float negA = (mA == -INFINITY) ? 0.f : -mA;
+            const float negB = (mB == -INFINITY) ? 0.f : -mB;
+            const uint64_t negA2 = f2_pack(negA, negA), negB2 = f2_pack(negB, negB);
+            // P = exp2(s * scale * log2e - m) as packed bf16 pairs, stored over the
+            // S columns (16x128b: repetition i of part q is P column 32q + 4i + cq,
+            // keys 64q + 8i + 2cq + {0, 1}).  Each part is signalled as soon as it
+            // is stored, so the MMA warp starts P V on it while the rest is computed.
             const bool any_rescale = __any_sync(0xffffffffu, rescale);
 #pragma unroll
             for (int hh = 0; hh < kPParts; ++hh) {
-                uint32_t pk[kPairsPerPart];
+                uint32_t pk[16];
 #pragma unroll
-                for (int i = 0; i < kPairsPerPart; ++i) {
-                    const int e = hh * 2 * kPairsPerPart + 2 * i;
-                    const uint64_t x2 = f2_fma(f2_pack_u(SR(e), SR(e + 1)), sl2_pair, negm_pair);
-                    float p0, p1;
-                    if (kSoftExpEvery > 0 && (i % (kSoftExpEvery > 0 ? kSoftExpEvery : 1)) ==
-                                                 kSoftExpEvery - 1) {
-                        // this pair on the FMA pipes, the rest on the exp unit
-                        const float2 pv = f2_unpack(exp2_fma_pair(x2));
-                        p0 = pv.x;
-                        p1 = pv.y;
-                    } else {
-                        const float2 x = f2_unpack(x2);
-                        p0 = ex2(x.x);
-                        p1 = ex2(x.y);
+                for (int i = 0; i < 8; ++i) {
+#pragma unroll
+                    for (int x = 0; x < 2; ++x) {  // row A, row B
+                        const int e = hh * 32 + 4 * i + 2 * x;
+                        const uint64_t x2 = f2_fma(f2_pack_u(SR(e), SR(e + 1)), sl2_pair,
+                                                   x == 0 ? negA2 : negB2);
+                        float p0, p1;
+                        const int pair = 2 * i + x;
+                        if (kSoftExpEvery > 0 &&
+                            (pair % (kSoftExpEvery > 0 ? kSoftExpEvery : 1)) == kSoftExpEvery - 1) {
+                            // this pair on the FMA pipes, the rest on the exp unit
+                            const float2 pv = f2_unpack(exp2_fma_pair(x2));
+                            p0 = pv.x;
+                            p1 = pv.y;
+                        } else {
+                            const float2 xv = f2_unpack(x2);
+                            p0 = ex2(xv.x);
+                            p1 = ex2(xv.y);
+                        }
+                        if (x == 0)
+                            lA = f2_add(lA, f2_pack(p0, p1));
+                        else
+                            lB = f2_add(lB, f2_pack(p0, p1));
+                        pk[2 * i + x] = pack_bf16x2(p0, p1);
                     }
-                    l_pair = f2_add(l_pair, f2_pack(p0, p1));
-                    pk[i] = pack_bf16x2(p0, p1);
                 }
-                tmem_st_cols<kPairsPerPart>(p_addr + hh * kPairsPerPart, pk);
+                tmem_st_16x128b_x8(s_addr + hh * 32, pk);
                 if (hh == 0 && any_rescale) {
                     // O already holds P V of earlier tiles: wait for the latest one,
                     // then rescale it before any of this tile's P V is issued.
                     ok = mbar_wait_warp(smem_u32(&sm.o_done[t]), (j - 1) & 1, kWaitTimeoutNs, abort);
                     if (!ok) break;
                     tc_fence_after();
-                    const uint64_t a2 = f2_pack(alpha, alpha);
+                    const uint64_t aA = f2_pack(alphaA, alphaA), aB = f2_pack(alphaB, alphaB);
 #pragma unroll
-                    for (int c = 0; c < kOH / 16; ++c) {
+                    for (int c = 0; c < HD / 32; ++c) {
                         uint32_t r[16];
-                        tmem_ld16(o_addr + c * 16, r);
+                        tmem_ld_16x256b_x4(o_addr + c * 32, r);
                         tmem_wait_ld();
                         reg_fence(r);
 #pragma unroll
                         for (int i = 0; i < 8; ++i) {
-                            const float2 v = f2_unpack(f2_mul(f2_pack_u(r[2 * i], r[2 * i + 1]), a2));
+                            const float2 v = f2_unpack(
+                                f2_mul(f2_pack_u(r[2 * i], r[2 * i + 1]), (i & 1) ? aB : aA));
                             r[2 * i] = __float_as_uint(v.x);
                             r[2 * i + 1] = __float_as_uint(v.y);
                         }
-                        tmem_st16(o_addr + c * 16, r);
+                        tmem_st_16x256b_x4(o_addr + c * 32, r);
                     }
                 }
                 tmem_wait_st();
@@ -463,49 +518,57 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
 #undef SR
             if (!ok) break;
             {
-                // the loop's rounding steps applied to this half's largest score
-                const float pmx = ex2(fmaf(pm, sl2, neg_m));
-                lc += __uint_as_float(pack_bf16x2(pmx, 0.f) << 16) - pmx;
+                // the loop's rounding steps applied to each row's largest score
+                const float pxA = ex2(fmaf(pmA, sl2, negA));
+                const float pxB = ex2(fmaf(pmB, sl2, negB));
+                const uint32_t pb = pack_bf16x2(pxA, pxB);
+                lcA += __uint_as_float(pb << 16) - pxA;
+                lcB += __uint_as_float(pb & 0xffff0000u) - pxB;
             }
         }
         if (!ok) {
             if (lane == 0) record_timeout(args, abort);
         } else if (my_nkv > 0) {
-            const float2 lp = f2_unpack(l_pair);
-            sm.xsum[t][half][0][row] = lp.x + lp.y;
-            sm.xsum[t][half][1][row] = lc;
-            mbar_arrive(smem_u32(&sm.xfin[t]));
-            ok = mbar_wait_warp(smem_u32(&sm.xfin[t]), 0, kWaitTimeoutNs, abort) &&
-                 mbar_wait_warp(smem_u32(&sm.o_done[t]), (my_nkv - 1) & 1, kWaitTimeoutNs, abort);
+            // full row sums across the row's four threads
+            const float2 la = f2_unpack(lA), lb = f2_unpack(lB);
+            float sA = la.x + la.y, sB = lb.x + lb.y;
+            sA += __shfl_xor_sync(0xffffffffu, sA, 1);
+            sB += __shfl_xor_sync(0xffffffffu, sB, 1);
+            sA += __shfl_xor_sync(0xffffffffu, sA, 2);
+            sB += __shfl_xor_sync(0xffffffffu, sB, 2);
+            ok = mbar_wait_warp(smem_u32(&sm.o_done[t]), (my_nkv - 1) & 1, kWaitTimeoutNs, abort);
             if (ok) {
                 tc_fence_after();
-                const float l_sum = sm.xsum[t][0][0][row] + sm.xsum[t][1][0][row];
-                const float l_round = l_sum + (sm.xsum[t][0][1][row] + sm.xsum[t][1][1][row]);
-                const float inv_l = 1.f / l_round;
-                const bool store = qi < N;
-                const size_t row_off = (static_cast<size_t>(bh) * N + qi) * HD + half * kOH;
-                uint8_t* orow = reinterpret_cast<uint8_t*>(args.o) + row_off * 2;
+                const float invA = 1.f / (sA + lcA), invB = 1.f / (sB + lcB);
+                const bool storeA = qA < N, storeB = qB < N;
+                uint8_t* oA = reinterpret_cast<uint8_t*>(args.o) +
+                              ((static_cast<size_t>(bh) * N + qA) * HD + 2 * cq) * 2;
+                uint8_t* oB = oA + static_cast<size_t>(8) * HD * 2;
 #pragma unroll
-                for (int c = 0; c < kOH / 32; ++c) {
-                    uint32_t r[32];
-                    tmem_ld32(o_addr + c * 32, r);
+                for (int c = 0; c < HD / 32; ++c) {
+                    uint32_t r[16];
+                    tmem_ld_16x256b_x4(o_addr + c * 32, r);
                     tmem_wait_ld();
                     reg_fence(r);
-                    uint32_t pk[16];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * inv_l,
-                                            __uint_as_float(r[2 * i + 1]) * inv_l);
-                    if (store) {
-#pragma unroll
-                        for (int v4 = 0; v4 < 4; ++v4)
-                            st_global_v4(orow + c * 64 + v4 * 16, pk[4 * v4], pk[4 * v4 + 1],
-                                         pk[4 * v4 + 2], pk[4 * v4 + 3]);
+                    for (int i = 0; i < 4; ++i) {
+                        const uint32_t wa = pack_bf16x2(__uint_as_float(r[4 * i]) * invA,
+                                                        __uint_as_float(r[4 * i + 1]) * invA);
+                        const uint32_t wb = pack_bf16x2(__uint_as_float(r[4 * i + 2]) * invB,
+                                                        __uint_as_float(r[4 * i + 3]) * invB);
+                        const int col = c * 32 + 8 * i;  // + 2cq, folded into oA / oB
+                        if (storeA) *reinterpret_cast<uint32_t*>(oA + col * 2) = wa;
+                        if (storeB) *reinterpret_cast<uint32_t*>(oB + col * 2) = wb;
                     }
                 }
-                if (store && half == 0)
-                    args.lse[static_cast<size_t>(bh) * N + qi] =
-                        (m_ref + __log2f(l_sum)) * 0.69314718055994531f;
+                if (cq == 0) {
+                    if (storeA)
+                        args.lse[static_cast<size_t>(bh) * N + qA] =
+                            (mA + __log2f(sA)) * 0.69314718055994531f;
+                    if (storeB)
+                        args.lse[static_cast<size_t>(bh) * N + qB] =
+                            (mB + __log2f(sB)) * 0.69314718055994531f;
+                }
             } else if (lane == 0) {
                 record_timeout(args, abort);
             }

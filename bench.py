@@ -1,7 +1,7 @@
 """Benchmark: exact attention fwd+bwd on GB300, TFLOP/s and % of dense BF16 peak.
 
-One step = the whole path on one batch: fa_fwd (O, lse) then fa_bwd (prep,
-main, finish -> dQ, dK, dV) on the workload B=4 H=16 N=4096 d=128, causal,
+One step = the whole path on one batch: fa_fwd (O, lse) then fa_bwd (prep ->
+D, main -> dK, dV, dq -> dQ) on the workload B=4 H=16 N=4096 d=128, causal,
 bf16 inputs resident in HBM.  FLOPs per step follow the convention
 4*B*H*N^2*d for the forward, halved for causal, and 2.5x that for the
 backward.  Prints one JSON line (rank 0).
@@ -39,7 +39,8 @@ def fwd_flops(w, causal=True):
     return 4.0 * w.B * w.H * w.N * w.N * w.d / (2.0 if causal else 1.0)
 
 
-KERNEL_SOURCES = {"fa_bwd_main_kernel<128>": ("fa_bwd.cu", "ptx.cuh", "fa_internal.cuh"),
+KERNEL_SOURCES = {"fa_bwd_dkdv_kernel<128>": ("fa_bwd.cu", "ptx.cuh", "fa_internal.cuh"),
+                  "fa_bwd_dq_kernel<128>": ("fa_bwd_dq.cu", "ptx.cuh", "fa_internal.cuh"),
                   "fa_fwd_kernel<128>": ("fa_fwd.cu", "ptx.cuh", "fa_internal.cuh")}
 
 
@@ -281,14 +282,15 @@ def run_gpu(args, world, rank, local):
         check(fa.fa_fwd(P(q), P(k), P(v), P(o), P(lse), B, H, N, d, scale, 1, h), "fa_fwd")
         if ev:
             ev[1].record(stream)
-        check(fa.fa_bwd_prep(P(o), P(do), B, H, N, d, P(ws), ws.numel(), h), "fa_bwd_prep")
+        check(fa.fa_bwd_prep(P(o), P(do), P(lse), B, H, N, d, P(ws), ws.numel(), h), "fa_bwd_prep")
         if ev:
             ev[2].record(stream)
         check(fa.fa_bwd_main(P(q), P(k), P(v), P(lse), P(do), P(dk), P(dv), B, H, N, d, scale, 1,
                              P(ws), ws.numel(), h), "fa_bwd_main")
         if ev:
             ev[3].record(stream)
-        check(fa.fa_bwd_finish(P(dq), B, H, N, d, P(ws), ws.numel(), h), "fa_bwd_finish")
+        check(fa.fa_bwd_dq(P(q), P(k), P(v), P(lse), P(do), P(dq), B, H, N, d, scale, 1, P(ws),
+                           ws.numel(), h), "fa_bwd_dq")
         if ev:
             ev[4].record(stream)
 
@@ -316,21 +318,24 @@ def run_gpu(args, world, rank, local):
     elapsed_ms = t_start.elapsed_time(t_end)
     elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
     per = {name: sum(e[a].elapsed_time(e[b]) for e in evs) / args.steps
-           for name, a, b in (("fwd", 0, 1), ("bwd_prep", 1, 2), ("bwd_main", 2, 3),
-                              ("bwd_finish", 3, 4))}
+           for name, a, b in (("fwd", 0, 1), ("bwd_prep", 1, 2), ("bwd_dkdv", 2, 3),
+                              ("bwd_dq", 3, 4))}
     f_fwd = fwd_flops(w)
     f_step = 3.5 * f_fwd
     value = f_step * args.steps * world / (elapsed_ms / 1e3) / 1e12
     ms_step = elapsed_ms / args.steps
 
-    # dominant kernel: the backward main kernel
+    # dominant kernel.  Algorithmic FLOPs per launch: the forward's two MMAs
+    # (S, P V) are f_fwd; the dK/dV kernel's four (S, dP, dV, dK) 2 f_fwd; the
+    # dQ kernel's dQ = dS K 0.5 f_fwd (its recomputed S and dP are overhead).
     dom = max(per, key=per.get)
-    dom_flops = {"fwd": f_fwd, "bwd_main": 2.5 * f_fwd}.get(dom)
+    dom_flops = {"fwd": f_fwd, "bwd_dkdv": 2.0 * f_fwd, "bwd_dq": 0.5 * f_fwd}.get(dom)
     achieved = dom_flops / (per[dom] / 1e3) / 1e12 if dom_flops else None
     peak_sus = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
     peak_burst = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
     roofline = {
-        "kernel": {"bwd_main": "fa_bwd_main_kernel<128>", "fwd": "fa_fwd_kernel<128>"}.get(dom, dom),
+        "kernel": {"bwd_dkdv": "fa_bwd_dkdv_kernel<128>", "bwd_dq": "fa_bwd_dq_kernel<128>",
+                   "fwd": "fa_fwd_kernel<128>"}.get(dom, dom),
         "bound": "tensor", "achieved": achieved, "peak": peak_sus, "unit": "TFLOP/s",
         "frac": achieved / peak_sus if achieved else None,
         "peak_kind": f"bf16_tflops_sustained ({peak_src}), the kernel runs inside a long step loop",
@@ -345,7 +350,8 @@ def run_gpu(args, world, rank, local):
     kname = roofline["kernel"]
     roofline["traffic"] = profiled_traffic(kname)
     if roofline["traffic"] is not None:
-        alg = {"fa_bwd_main_kernel<128>": (16 * w.N * w.d + 12 * w.N) * w.B * w.H,
+        alg = {"fa_bwd_dkdv_kernel<128>": (12 * w.N * w.d + 8 * w.N) * w.B * w.H,
+               "fa_bwd_dq_kernel<128>": (10 * w.N * w.d + 8 * w.N) * w.B * w.H,
                "fa_fwd_kernel<128>": (8 * w.N * w.d + 4 * w.N) * w.B * w.H}.get(kname)
         roofline["algorithmic_bytes"] = alg
         roofline["traffic_over_algorithmic"] = roofline["traffic"] / alg if alg else None
@@ -461,7 +467,7 @@ def run_gpu(args, world, rank, local):
 def run_only(args, local):
     """Untimed launches of one part of the path, for profilers: `fwd` runs the
     forward on the N=8192 d=128 K x3 causal workload, `fwd64` the non-causal
-    forward on B=4 H=16 N=2048 d=64, `bwd` the backward (prep, main, finish)
+    forward on B=4 H=16 N=2048 d=64, `bwd` the backward (prep, main, dq)
     on the fwd+bwd workload.  W + K launches each."""
     import torch
     import exact_tiled_attention_05_gb300 as fa

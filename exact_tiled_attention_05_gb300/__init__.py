@@ -25,7 +25,7 @@ FA_ERR_DEVICE_TIMEOUT = 6
 
 EXPORTED = (
     "fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_bwd_prep", "fa_bwd_main",
-    "fa_bwd_finish", "fa_bwd_noalloc", "fa_sync_status", "fa_status_string", "fa_version",
+    "fa_bwd_dq", "fa_bwd_noalloc", "fa_sync_status", "fa_status_string", "fa_version",
 )
 
 _lib = None
@@ -52,9 +52,9 @@ def load_library(path: str = LIB_PATH):
         "fa_fwd": ([P, P, P, P, P, I, I, I, I, F, I, P], I),
         "fa_bwd_workspace_size": ([I, I, I, I], Z),
         "fa_bwd": ([P, P, P, P, P, P, P, P, P, I, I, I, I, F, I, P, Z, P], I),
-        "fa_bwd_prep": ([P, P, I, I, I, I, P, Z, P], I),
+        "fa_bwd_prep": ([P, P, P, I, I, I, I, P, Z, P], I),
         "fa_bwd_main": ([P, P, P, P, P, P, P, I, I, I, I, F, I, P, Z, P], I),
-        "fa_bwd_finish": ([P, I, I, I, I, P, Z, P], I),
+        "fa_bwd_dq": ([P, P, P, P, P, P, I, I, I, I, F, I, P, Z, P], I),
         "fa_bwd_noalloc": ([P, P, P, P, P, P, P, P, P, I, I, I, I, F, I, P], I),
         "fa_sync_status": ([P], I),
         "fa_status_string": ([I], ctypes.c_char_p),
@@ -85,8 +85,8 @@ def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, causal, ws, ws_
                                  ws, ws_bytes, stream)
 
 
-def fa_bwd_prep(o, dout, B, H, N, d, ws, ws_bytes, stream):
-    return load_library().fa_bwd_prep(o, dout, B, H, N, d, ws, ws_bytes, stream)
+def fa_bwd_prep(o, dout, lse, B, H, N, d, ws, ws_bytes, stream):
+    return load_library().fa_bwd_prep(o, dout, lse, B, H, N, d, ws, ws_bytes, stream)
 
 
 def fa_bwd_main(q, k, v, lse, dout, dk, dv, B, H, N, d, scale, causal, ws, ws_bytes, stream):
@@ -94,8 +94,9 @@ def fa_bwd_main(q, k, v, lse, dout, dk, dv, B, H, N, d, scale, causal, ws, ws_by
                                       ws, ws_bytes, stream)
 
 
-def fa_bwd_finish(dq, B, H, N, d, ws, ws_bytes, stream):
-    return load_library().fa_bwd_finish(dq, B, H, N, d, ws, ws_bytes, stream)
+def fa_bwd_dq(q, k, v, lse, dout, dq, B, H, N, d, scale, causal, ws, ws_bytes, stream):
+    return load_library().fa_bwd_dq(q, k, v, lse, dout, dq, B, H, N, d, scale, causal, ws,
+                                    ws_bytes, stream)
 
 
 def fa_bwd_noalloc(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, causal, stream):

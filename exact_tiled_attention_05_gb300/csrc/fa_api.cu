@@ -109,23 +109,6 @@ int make_map(CUtensorMap* map, const void* ptr, int BH, int N, int d) {
     return r == CUDA_SUCCESS ? kOk : kErrCuda;
 }
 
-// fp32 [BH, N, d] accumulator -> 3-D map, box 32 x 128 x 1 (128-byte rows),
-// 128 B swizzle: the layout the dQ reduce stages in shared memory.
-int make_map_f32(CUtensorMap* map, const void* ptr, int BH, int N, int d) {
-    EncodeTiledFn enc = encode_fn();
-    if (!enc) return kErrCuda;
-    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
-                          static_cast<cuuint64_t>(BH)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4,
-                             static_cast<cuuint64_t>(d) * 4 * static_cast<cuuint64_t>(N)};
-    cuuint32_t box[3] = {32, 128, 1};
-    cuuint32_t elem[3] = {1, 1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(ptr), dims,
-                     strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? kOk : kErrCuda;
-}
-
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int check_shape(int B, int H, int N, int d, float scale, int causal) {
@@ -140,18 +123,12 @@ int check_shape(int B, int H, int N, int d, float scale, int causal) {
 
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
-struct WorkspaceLayout {
-    size_t dq_acc_off, delta_off, total;
-};
-
-WorkspaceLayout ws_layout(int B, int H, int N, int d) {
-    const size_t rows = static_cast<size_t>(B) * H * N;
-    WorkspaceLayout w{};
-    w.dq_acc_off = 0;
-    w.delta_off = round256(rows * d * sizeof(float));
-    w.total = w.delta_off + round256(rows * sizeof(float));
-    return w;
+// The backward's scratch: D = rowsum(dO * O) and lse * log2(e), each fp32
+// [B*H, rows padded to whole 128-row tiles].
+size_t ws_half(int B, int H, int N) {
+    return round256(static_cast<size_t>(B) * H * ((N + 127) / 128) * 128 * sizeof(float));
 }
+size_t ws_bytes(int B, int H, int N) { return 2 * ws_half(B, H, N); }
 
 int map_cuda(cudaError_t e) { return e == cudaSuccess ? kOk : kErrCuda; }
 
@@ -162,21 +139,44 @@ int bwd_common(BwdArgs& a, int B, int H, int N, int d, float scale, int causal, 
     if (rc) return rc;
     if (!workspace) return kErrWorkspace;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return kErrWorkspace;
-    const WorkspaceLayout w = ws_layout(B, H, N, d);
-    if (workspace_bytes < w.total) return kErrWorkspace;
-    a.dq_acc = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + w.dq_acc_off);
-    a.delta = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + w.delta_off);
+    if (workspace_bytes < ws_bytes(B, H, N)) return kErrWorkspace;
+    a.delta = static_cast<float*>(workspace);
+    a.lse2 = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + ws_half(B, H, N));
     a.BH = B * H;
     a.N = N;
     a.n_kblk = (N + 127) / 128;
     a.causal = causal;
     rc = device_ready(&a.status);
     if (rc) return rc;
-    // about 0.9 wave of CTAs per head group, rounded down to a power of two
-    // (measured best: 4 heads on the N = 4096 workload)
+    // dK/dV kernel: about 0.9 wave of CTAs per head group, rounded down to a
+    // power of two (measured best: 4 heads on the N = 4096 workload); dQ
+    // kernel: about two waves, as the forward
     a.group = clampi(floor_pow2(clampi((current_sms() * 9 / 10) / a.n_kblk, 1, 1 << 20)), 1, a.BH);
+    a.group_dq = clampi(floor_pow2(clampi((2 * current_sms()) / a.n_kblk, 1, 1 << 20)), 1, a.BH);
     a.scale = scale;
     a.scale_log2 = scale * 1.4426950408889634f;
+    return kOk;
+}
+
+// Shared by the dK/dV and dQ stages: validates, fills BwdArgs and the four
+// bf16 tensor maps.
+int bwd_maps(BwdArgs& a, CUtensorMap* maps, const void* q, const void* k, const void* v,
+             const float* lse, const void* dout, int B, int H, int N, int d, float scale,
+             int causal, void* workspace, size_t workspace_bytes) {
+    int rc = bwd_common(a, B, H, N, d, scale, causal, workspace, workspace_bytes);
+    if (rc) return rc;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dout) ||
+        (reinterpret_cast<uintptr_t>(lse) & 3u))
+        return kErrMisaligned;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.lse = lse;
+    a.dout = dout;
+    const int BH = B * H;
+    if ((rc = make_map(&maps[0], q, BH, N, d)) || (rc = make_map(&maps[1], k, BH, N, d)) ||
+        (rc = make_map(&maps[2], v, BH, N, d)) || (rc = make_map(&maps[3], dout, BH, N, d)))
+        return rc;
     return kOk;
 }
 
@@ -187,7 +187,7 @@ using namespace fa;
 
 extern "C" {
 
-int fa_version(void) { return 100; }
+int fa_version(void) { return 200; }
 
 const char* fa_status_string(int status) {
     switch (status) {
@@ -232,18 +232,20 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
 
 size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
     if (B < 1 || H < 1 || N < 1 || d < 1) return 0;
-    return ws_layout(B, H, N, d).total;
+    return ws_bytes(B, H, N);
 }
 
-int fa_bwd_prep(const void* o, const void* dout, int B, int H, int N, int d, void* workspace,
-                size_t workspace_bytes, void* stream) {
-    if (!o || !dout) return FA_ERR_INVALID_ARG;
+int fa_bwd_prep(const void* o, const void* dout, const float* lse, int B, int H, int N, int d,
+                void* workspace, size_t workspace_bytes, void* stream) {
+    if (!o || !dout || !lse) return FA_ERR_INVALID_ARG;
     BwdArgs a{};
     int rc = bwd_common(a, B, H, N, d, 1.f, 0, workspace, workspace_bytes);
     if (rc) return rc;
-    if (!aligned16(o) || !aligned16(dout)) return FA_ERR_MISALIGNED;
+    if (!aligned16(o) || !aligned16(dout) || (reinterpret_cast<uintptr_t>(lse) & 3u))
+        return FA_ERR_MISALIGNED;
     a.o = o;
     a.dout = dout;
+    a.lse = lse;
     return map_cuda(launch_bwd_prep(d, a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -252,37 +254,28 @@ int fa_bwd_main(const void* q, const void* k, const void* v, const float* lse, c
                 void* workspace, size_t workspace_bytes, void* stream) {
     if (!q || !k || !v || !lse || !dout || !dk || !dv) return FA_ERR_INVALID_ARG;
     BwdArgs a{};
-    int rc = bwd_common(a, B, H, N, d, scale, causal, workspace, workspace_bytes);
+    CUtensorMap m[4];
+    int rc = bwd_maps(a, m, q, k, v, lse, dout, B, H, N, d, scale, causal, workspace,
+                      workspace_bytes);
     if (rc) return rc;
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dout) || !aligned16(dk) ||
-        !aligned16(dv) || (reinterpret_cast<uintptr_t>(lse) & 3u))
-        return FA_ERR_MISALIGNED;
-    a.q = q;
-    a.k = k;
-    a.v = v;
-    a.lse = lse;
-    a.dout = dout;
+    if (!aligned16(dk) || !aligned16(dv)) return FA_ERR_MISALIGNED;
     a.dk = dk;
     a.dv = dv;
-    CUtensorMap tq, tk, tv, tdo, tdq;
-    const int BH = B * H;
-    if ((rc = make_map(&tq, q, BH, N, d)) || (rc = make_map(&tk, k, BH, N, d)) ||
-        (rc = make_map(&tv, v, BH, N, d)) || (rc = make_map(&tdo, dout, BH, N, d)) ||
-        (rc = make_map_f32(&tdq, a.dq_acc, BH, N, d)))
-        return rc;
-    return map_cuda(
-        launch_bwd_main(d, tq, tk, tv, tdo, tdq, a, static_cast<cudaStream_t>(stream)));
+    return map_cuda(launch_bwd_dkdv(d, m[0], m[1], m[2], m[3], a, static_cast<cudaStream_t>(stream)));
 }
 
-int fa_bwd_finish(void* dq, int B, int H, int N, int d, void* workspace, size_t workspace_bytes,
-                  void* stream) {
-    if (!dq) return FA_ERR_INVALID_ARG;
+int fa_bwd_dq(const void* q, const void* k, const void* v, const float* lse, const void* dout,
+              void* dq, int B, int H, int N, int d, float scale, int causal, void* workspace,
+              size_t workspace_bytes, void* stream) {
+    if (!q || !k || !v || !lse || !dout || !dq) return FA_ERR_INVALID_ARG;
     BwdArgs a{};
-    int rc = bwd_common(a, B, H, N, d, 1.f, 0, workspace, workspace_bytes);
+    CUtensorMap m[4];
+    int rc = bwd_maps(a, m, q, k, v, lse, dout, B, H, N, d, scale, causal, workspace,
+                      workspace_bytes);
     if (rc) return rc;
     if (!aligned16(dq)) return FA_ERR_MISALIGNED;
     a.dq = dq;
-    return map_cuda(launch_bwd_finish(d, a, static_cast<cudaStream_t>(stream)));
+    return map_cuda(launch_bwd_dq(d, m[0], m[1], m[2], m[3], a, static_cast<cudaStream_t>(stream)));
 }
 
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
@@ -291,11 +284,12 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
     if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
     int rc = check_shape(B, H, N, d, scale, causal);
     if (rc) return rc;
-    if ((rc = fa_bwd_prep(o, dout, B, H, N, d, workspace, workspace_bytes, stream))) return rc;
+    if ((rc = fa_bwd_prep(o, dout, lse, B, H, N, d, workspace, workspace_bytes, stream))) return rc;
     if ((rc = fa_bwd_main(q, k, v, lse, dout, dk, dv, B, H, N, d, scale, causal, workspace,
                           workspace_bytes, stream)))
         return rc;
-    return fa_bwd_finish(dq, B, H, N, d, workspace, workspace_bytes, stream);
+    return fa_bwd_dq(q, k, v, lse, dout, dq, B, H, N, d, scale, causal, workspace, workspace_bytes,
+                     stream);
 }
 
 int fa_sync_status(void* stream) {

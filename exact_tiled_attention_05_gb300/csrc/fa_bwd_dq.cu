@@ -1,0 +1,364 @@
+// fa_bwd_dq.cu -- dQ kernel of the backward pass for sm_103a.
+#include "fa_internal.cuh"
+#include "ptx.cuh"
+
+namespace fa {
+namespace {
+
+using namespace ptx;
+
+// ---------------------------------------------------------------------------
+// dQ: one CTA per (head, 128-row query tile i), looping over 128-key tiles j
+// (j <= i when causal), with dQ_i accumulated in TMEM for the whole loop:
+//   S    = Q_i K_j^T                  (TMEM, fp32; two buffers)
+//   dP   = dO_i V_j^T                 (TMEM, fp32)
+//   P    = exp2(S * scale*log2e - lse_i * log2e)       (recomputed from lse)
+//   dS   = P * (dP - D_i)             (bf16, written over S's columns)
+//   dQ_i += dS K_j                    (dS from TMEM, K_j MN-major)
+//   dq_i  = bf16(scale * dQ_i)
+// The same formulas as the dK/dV kernel (the softmax Jacobian), with query
+// rows on the MMA M dimension: lse_i and D_i are per-row constants, so a
+// thread needs no exchange with the other thread of its row.  S and dP are
+// recomputed here rather than sending a partial dQ per (i, j) tile out of
+// the SM (see the dK/dV kernel).
+// MMA issue order per key tile: S(j) into buffer j%2, dP(j), dQ(j-1).  S(j+1)
+// only has to wait for dQ(j-1) to have consumed dS(j-1) from the same buffer,
+// so the compute warps find S and dP of the next tile ready.
+// Roles: warp 0 TMA, warp 1 MMA + TMEM allocation, warps 2-5
+// / 6-9 compute for key columns 0-63 / 64-127 of each tile.
+// ---------------------------------------------------------------------------
+constexpr int kQThreads = 320;
+constexpr int kQCompute = 256;       // threads of warps 2..9; each arrives on the compute barriers
+constexpr int kQBox = 128 * 64 * 2;  // one 64-column box of a 128-row bf16 tile
+
+template <int HD>
+struct DqCfg {
+    static constexpr int kTile = 128 * HD * 2;
+    static constexpr int kBoxes = HD / 64;
+    static constexpr int kStages = HD == 128 ? 5 : 10;  // K/V ring slots (K_j, V_j alternate)
+    static constexpr uint32_t kS = 0;     // S / dS buffers at columns 0 and 128
+    static constexpr uint32_t kDP = 256;
+    static constexpr uint32_t kDQ = 384;
+    static constexpr uint32_t kTmemCols = 512;
+};
+
+template <int HD>
+struct alignas(1024) DqSmem {
+    uint8_t q[DqCfg<HD>::kTile];
+    uint8_t dout[DqCfg<HD>::kTile];
+    uint8_t kv[DqCfg<HD>::kStages][DqCfg<HD>::kTile];
+    float lse2[128];   // lse * log2(e) per query row (+inf past the end)
+    float delta[128];  // D per query row
+    uint64_t qd_full;  // Q, dO and their lse * log2(e), D landed
+    uint64_t kv_full[DqCfg<HD>::kStages];
+    uint64_t kv_empty[DqCfg<HD>::kStages];
+    uint64_t s_full[2];    // per S buffer
+    uint64_t dp_full;
+    uint64_t dp_free;      // the compute warps have read dP
+    uint64_t ds_ready[2];  // per S buffer: dS written over it
+    uint64_t dq_done;
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+};
+
+static_assert(sizeof(DqSmem<128>) <= 232448, "dQ kernel d=128 shared memory exceeds 227 KB");
+static_assert(sizeof(DqSmem<64>) <= 232448, "dQ kernel d=64 shared memory exceeds 227 KB");
+
+__device__ __forceinline__ void dq_timeout(const BwdArgs& a, volatile int* abort) {
+    *abort = 1;
+    atomicExch(a.status, kErrDeviceTimeout);
+}
+
+template <int HD>
+__global__ void __launch_bounds__(kQThreads, 1)
+fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                 const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+                 const BwdArgs a) {
+    using Cfg = DqCfg<HD>;
+    extern __shared__ __align__(1024) uint8_t qsmem_raw[];
+    if ((smem_u32(qsmem_raw) & 1023u) != 0u) {  // the swizzled layouts need 1 KB alignment
+        if (threadIdx.x == 0) atomicExch(a.status, kErrUnsupported);
+        return;
+    }
+    DqSmem<HD>& sm = *reinterpret_cast<DqSmem<HD>*>(qsmem_raw);
+    volatile int* abort = &sm.abort;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int N = a.N;
+    const int nq = a.n_kblk;  // query tiles == key tiles (both 128 rows)
+    int bh, i;
+    if (a.causal) {
+        // groups of a.group_dq heads; inside a group the query tiles with the
+        // most key tiles (large i) launch first
+        const int b = static_cast<int>(blockIdx.x);
+        const int grp = b / (a.group_dq * nq);
+        const int first = grp * a.group_dq;
+        const int gc = min(a.group_dq, a.BH - first);
+        const int r = b - grp * a.group_dq * nq;
+        i = nq - 1 - r / gc;
+        bh = first + r % gc;
+    } else {
+        bh = static_cast<int>(blockIdx.x) / nq;
+        i = static_cast<int>(blockIdx.x) % nq;
+    }
+    const int q0 = i * 128;
+    const int n = a.causal ? i + 1 : nq;  // key tiles
+
+    if (threadIdx.x == 0) {
+        sm.abort = 0;
+        mbar_init(smem_u32(&sm.qd_full), 1);
+        for (int s = 0; s < Cfg::kStages; ++s) {
+            mbar_init(smem_u32(&sm.kv_full[s]), 1);
+            mbar_init(smem_u32(&sm.kv_empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&sm.s_full[b]), 1);
+            mbar_init(smem_u32(&sm.ds_ready[b]), kQCompute);
+        }
+        mbar_init(smem_u32(&sm.dp_full), 1);
+        mbar_init(smem_u32(&sm.dp_free), kQCompute);
+        mbar_init(smem_u32(&sm.dq_done), 1);
+        mbar_init(smem_u32(&sm.drain), 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&sm.tmem_base), Cfg::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = sm.tmem_base;
+
+    if (warp == 0) {
+        // ===================== loads =====================
+        const bool leader = lane == 0;
+        const uint32_t qbar = smem_u32(&sm.qd_full);
+        if (leader) {
+            tma_prefetch_desc(&tq);
+            tma_prefetch_desc(&tk);
+            tma_prefetch_desc(&tv);
+            tma_prefetch_desc(&tdo);
+            mbar_arrive_expect_tx(qbar, 2 * Cfg::kTile + 1024);
+            for (int b = 0; b < Cfg::kBoxes; ++b) {
+                tma_load_3d(smem_u32(sm.q + b * kQBox), &tq, qbar, b * 64, q0, bh);
+                tma_load_3d(smem_u32(sm.dout + b * kQBox), &tdo, qbar, b * 64, q0, bh);
+            }
+            // the tile's lse * log2(e) and D (rows past the end: +inf and 0,
+            // written by the prep stage)
+            const size_t stat = static_cast<size_t>(bh) * nq * 128 + q0;
+            bulk_load(smem_u32(sm.lse2), a.lse2 + stat, 512, qbar);
+            bulk_load(smem_u32(sm.delta), a.delta + stat, 512, qbar);
+            // K_j and V_j stream through the ring: K_j is copy 2j, V_j copy 2j + 1.
+            const int n_loads = FA_FAULT_INJECT ? 0 : 2 * n;
+            bool ok = true;
+            int issued = 0;
+            for (int idx = 0; idx < n_loads; ++idx) {
+                const int slot = idx % Cfg::kStages;
+                if (!(ok = mbar_wait(smem_u32(&sm.kv_empty[slot]), ((idx / Cfg::kStages) & 1) ^ 1,
+                                     kWaitTimeoutNs, abort)))
+                    break;
+                const uint32_t bar = smem_u32(&sm.kv_full[slot]);
+                mbar_arrive_expect_tx(bar, Cfg::kTile);
+                const CUtensorMap* map = (idx & 1) ? &tv : &tk;
+                for (int b = 0; b < Cfg::kBoxes; ++b)
+                    tma_load_3d(smem_u32(sm.kv[slot] + b * kQBox), map, bar, b * 64, (idx >> 1) * 128, bh);
+                ++issued;
+            }
+            if (!ok) dq_timeout(a, abort);
+            // Let every copy that was issued land before the CTA can exit.
+            for (int slot = 0; slot < Cfg::kStages && slot < issued; ++slot) {
+                const int last = slot + Cfg::kStages * ((issued - 1 - slot) / Cfg::kStages);
+                mbar_wait_drain(smem_u32(&sm.kv_full[slot]), (last / Cfg::kStages) & 1, kWaitTimeoutNs);
+            }
+            mbar_wait_drain(qbar, 0, kWaitTimeoutNs);
+        }
+    } else if (warp == 1) {
+        // ===================== MMA issuer =====================
+        if (elect_one()) {
+            constexpr uint32_t id_kk = idesc_bf16_f32(128, 128, 0, 0);  // S, dP
+            constexpr uint32_t id_dq = idesc_bf16_f32(128, HD, 0, 1);   // dQ: dS from TMEM, K MN-major
+            const uint32_t q_addr = smem_u32(sm.q), do_addr = smem_u32(sm.dout);
+            auto wait_kv = [&](int idx) -> bool {
+                return mbar_wait(smem_u32(&sm.kv_full[idx % Cfg::kStages]), (idx / Cfg::kStages) & 1,
+                                 kWaitTimeoutNs, abort);
+            };
+            auto kv_addr = [&](int idx) -> uint32_t { return smem_u32(sm.kv[idx % Cfg::kStages]); };
+            // D[tmem] = A B^T with both operands K-major over the head dimension.
+            auto gemm_kk = [&](uint32_t d_col, uint32_t a_addr, uint32_t b_addr) {
+#pragma unroll
+                for (int kk = 0; kk < HD / 16; ++kk) {
+                    const uint32_t off = (kk / 4) * kQBox + (kk % 4) * 32;
+                    umma_ss(tbase + d_col, sdesc_sw128(a_addr + off, 16, 1024),
+                            sdesc_sw128(b_addr + off, 16, 1024), id_kk, kk > 0);
+                }
+            };
+            // dQ += dS(j) K_j : dS (bf16) from TMEM, keys 0-63 packed at columns
+            // [0,32) of its buffer, keys 64-127 at [64,96); K_j MN-major.
+            auto issue_dq = [&](int j) -> bool {
+                if (!mbar_wait(smem_u32(&sm.ds_ready[j & 1]), (j >> 1) & 1, kWaitTimeoutNs, abort))
+                    return false;
+                tc_fence_after();
+                const uint32_t buf = Cfg::kS + static_cast<uint32_t>(j & 1) * 128;
+                const uint32_t k_addr = kv_addr(2 * j);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t acol = buf + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
+                    umma_ts(tbase + Cfg::kDQ, tbase + acol, sdesc_sw128(k_addr + kk * 2048, kQBox, 1024),
+                            id_dq, (j > 0 || kk > 0) ? 1u : 0u);
+                }
+                umma_commit(smem_u32(&sm.kv_empty[(2 * j) % Cfg::kStages]));  // K_j read
+                return true;
+            };
+            bool ok = mbar_wait(smem_u32(&sm.qd_full), 0, kWaitTimeoutNs, abort);
+            for (int j = 0; ok && j < n; ++j) {
+                // S(j) into buffer j%2: dS(j-2) there was consumed by dQ(j-2),
+                // issued earlier (the tensor pipe runs one thread's MMAs in order).
+                if (!(ok = wait_kv(2 * j))) break;
+                tc_fence_after();
+                gemm_kk(Cfg::kS + static_cast<uint32_t>(j & 1) * 128, q_addr, kv_addr(2 * j));
+                umma_commit(smem_u32(&sm.s_full[j & 1]));
+                // dP(j): the compute warps have read dP(j-1)
+                if (j > 0 && !(ok = mbar_wait(smem_u32(&sm.dp_free), (j - 1) & 1, kWaitTimeoutNs, abort)))
+                    break;
+                if (!(ok = wait_kv(2 * j + 1))) break;
+                tc_fence_after();
+                gemm_kk(Cfg::kDP, do_addr, kv_addr(2 * j + 1));
+                umma_commit(smem_u32(&sm.dp_full));
+                umma_commit(smem_u32(&sm.kv_empty[(2 * j + 1) % Cfg::kStages]));  // V_j read
+                if (j > 0 && !(ok = issue_dq(j - 1))) break;
+            }
+            if (ok && n > 0) ok = issue_dq(n - 1);
+            if (!ok) dq_timeout(a, abort);
+            umma_commit(smem_u32(&sm.dq_done));
+            // Every MMA (and every commit before it) completes before the CTA leaves.
+            umma_commit(smem_u32(&sm.drain));
+            mbar_wait_drain(smem_u32(&sm.drain), 0, kWaitTimeoutNs);
+        }
+    } else {
+        // ===================== compute =====================
+        const int half = (warp - 2) >> 2;  // key columns [64 half, 64 half + 64) of S / dP
+        const int wq = warp & 3;           // TMEM lane quarter this warp may access
+        const int row = wq * 32 + lane;    // TMEM lane = query row of the tile
+        const int qi = q0 + row;
+        const uint32_t lane_addr = tbase + (static_cast<uint32_t>(wq * 32) << 16);
+        const float sl2 = a.scale_log2;
+        bool ok = mbar_wait_warp(smem_u32(&sm.qd_full), 0, kWaitTimeoutNs, abort);
+        const float lse2 = ok ? sm.lse2[row] : 0.f;
+        const float dval = ok ? sm.delta[row] : 0.f;
+        for (int j = 0; ok && j < n; ++j) {
+            const uint32_t buf = Cfg::kS + static_cast<uint32_t>(j & 1) * 128 + half * 64;
+            if (!(ok = mbar_wait_warp(smem_u32(&sm.s_full[j & 1]), (j >> 1) & 1, kWaitTimeoutNs, abort)))
+                break;
+            tc_fence_after();
+            float p[64];
+            {
+                uint32_t r0[32], r1[32];
+                tmem_ld32(lane_addr + buf, r0);
+                tmem_ld32(lane_addr + buf + 32, r1);
+                tmem_wait_ld();
+                reg_fence(r0);
+                reg_fence(r1);
+#pragma unroll
+                for (int c = 0; c < 64; ++c)
+                    p[c] = ex2(fmaf(__uint_as_float(c < 32 ? r0[c] : r1[c - 32]), sl2, -lse2));
+            }
+            const int kbase = j * 128 + half * 64;
+            if ((j * 128 + 128 > N) || (a.causal && j * 128 + 127 > q0)) {
+                const int kend = a.causal ? min(N, qi + 1) : N;
+#pragma unroll
+                for (int c = 0; c < 64; ++c)
+                    if (kbase + c >= kend) p[c] = 0.f;
+            }
+            if (!(ok = mbar_wait_warp(smem_u32(&sm.dp_full), j & 1, kWaitTimeoutNs, abort))) break;
+            tc_fence_after();
+            uint32_t pk[32];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t r[32];
+                tmem_ld32(lane_addr + Cfg::kDP + half * 64 + h * 32, r);
+                tmem_wait_ld();
+                reg_fence(r);
+                if (h == 1) {
+                    tc_fence_before();
+                    mbar_arrive(smem_u32(&sm.dp_free));
+                }
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    const int e = h * 32 + 2 * c;
+                    pk[h * 16 + c] = pack_bf16x2(p[e] * (__uint_as_float(r[2 * c]) - dval),
+                                                 p[e + 1] * (__uint_as_float(r[2 * c + 1]) - dval));
+                }
+            }
+            // dS over the first 32 columns this thread read: keys 64 half + [0, 64)
+            tmem_st32(lane_addr + buf, pk);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(smem_u32(&sm.ds_ready[j & 1]));
+        }
+        if (!ok) {
+            if (lane == 0) dq_timeout(a, abort);
+        } else {
+            ok = mbar_wait_warp(smem_u32(&sm.dq_done), 0, kWaitTimeoutNs, abort);
+            if (ok) {
+                tc_fence_after();
+                constexpr int kHalf = HD / 2;
+                const bool store = qi < N;
+                const size_t off = (static_cast<size_t>(bh) * N + qi) * HD + half * kHalf;
+                uint8_t* dst = static_cast<uint8_t*>(a.dq) + off * 2;
+#pragma unroll 1
+                for (int c = 0; c < kHalf; c += 32) {
+                    uint32_t r[32];
+                    tmem_ld32(lane_addr + Cfg::kDQ + half * kHalf + c, r);
+                    tmem_wait_ld();
+                    reg_fence(r);
+                    uint32_t w[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        w[e] = pack_bf16x2(a.scale * __uint_as_float(r[2 * e]),
+                                           a.scale * __uint_as_float(r[2 * e + 1]));
+                    if (store) {
+#pragma unroll
+                        for (int v4 = 0; v4 < 4; ++v4)
+                            st_global_v4(dst + c * 2 + v4 * 16, w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2],
+                                         w[4 * v4 + 3]);
+                    }
+                }
+            } else if (lane == 0) {
+                dq_timeout(a, abort);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tbase, Cfg::kTmemCols);
+    }
+}
+
+template <int HD>
+cudaError_t launch_bwd_dq_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t stream) {
+    const size_t smem = sizeof(DqSmem<HD>);
+    cudaError_t e = cudaFuncSetAttribute(fa_bwd_dq_kernel<HD>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    const unsigned grid = static_cast<unsigned>(a.n_kblk) * static_cast<unsigned>(a.BH);
+    fa_bwd_dq_kernel<HD><<<grid, kQThreads, smem, stream>>>(tq, tk, tv, tdo, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_dq(int d, const CUtensorMap& tq, const CUtensorMap& tk,
+                          const CUtensorMap& tv, const CUtensorMap& tdo, const BwdArgs& a,
+                          cudaStream_t stream) {
+    if (d == 64) return launch_bwd_dq_t<64>(tq, tk, tv, tdo, a, stream);
+    return launch_bwd_dq_t<128>(tq, tk, tv, tdo, a, stream);
+}
+
+}  // namespace fa

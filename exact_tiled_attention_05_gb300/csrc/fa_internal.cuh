@@ -28,7 +28,7 @@ enum : int {
 constexpr uint64_t kWaitTimeoutNs = FA_WAIT_TIMEOUT_NS;
 
 // Test builds only (never set by the library build): with FA_FAULT_INJECT=1 the
-// load warps never issue their K/V (forward) or Q/dO (backward) copies, so a
+// load warps never issue their K/V (forward, dQ kernel) or Q/dO (dK/dV kernel) copies, so a
 // bounded wait runs out and the kernel must report FA_ERR_DEVICE_TIMEOUT and
 // leave cleanly.  No fault, trap or endless wait is involved.
 #ifndef FA_FAULT_INJECT
@@ -57,12 +57,14 @@ struct BwdArgs {
     void* dq;
     void* dk;
     void* dv;
-    float* dq_acc;    // fp32 [BH, N, d] workspace
-    float* delta;     // fp32 [BH, N] workspace: rowsum(dO * O)
+    // workspace, fp32 [BH, n_kblk * 128] (rows padded to whole 128-row tiles):
+    float* delta;     // D = rowsum(dO * O); 0 in the padding
+    float* lse2;      // lse * log2(e); +inf in the padding (P = 0 there)
     int BH;
     int N;
-    int n_kblk;       // key blocks (128 rows) per head
-    int group;        // causal launch order: heads per group (heavy blocks first within a group)
+    int n_kblk;       // 128-row key blocks per head (= 128-row query blocks)
+    int group;        // causal launch order of the dK/dV kernel: heads per group
+    int group_dq;     // causal launch order of the dQ kernel: heads per group
     int causal;
     float scale;
     float scale_log2;
@@ -79,9 +81,11 @@ struct TensorMaps3 {
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const FwdArgs& args, cudaStream_t stream);
 cudaError_t launch_bwd_prep(int d, const BwdArgs& args, cudaStream_t stream);
-cudaError_t launch_bwd_main(int d, const CUtensorMap& tq, const CUtensorMap& tk,
-                            const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
-                            const BwdArgs& args, cudaStream_t stream);
-cudaError_t launch_bwd_finish(int d, const BwdArgs& args, cudaStream_t stream);
+cudaError_t launch_bwd_dkdv(int d, const CUtensorMap& tq, const CUtensorMap& tk,
+                            const CUtensorMap& tv, const CUtensorMap& tdo, const BwdArgs& args,
+                            cudaStream_t stream);
+cudaError_t launch_bwd_dq(int d, const CUtensorMap& tq, const CUtensorMap& tk,
+                          const CUtensorMap& tv, const CUtensorMap& tdo, const BwdArgs& args,
+                          cudaStream_t stream);
 
 }  // namespace fa

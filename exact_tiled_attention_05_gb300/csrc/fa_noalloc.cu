@@ -1,8 +1,8 @@
 // fa_noalloc.cu -- a backward pass for callers that cannot allocate device
 // memory.
 //
-// fa_bwd needs a scratch workspace (an fp32 dQ accumulator and the row
-// statistic D) that the caller allocates.  Some callers cannot do that: code
+// fa_bwd needs a scratch workspace (two fp32 row statistics) that the caller
+// allocates.  Some callers cannot do that: code
 // that runs where cudaMalloc is unavailable or forbidden (inside a custom
 // allocator's own callbacks, a fixed-footprint embedded service that must not
 // grow its memory after start-up, or a plug-in whose host framework owns every
@@ -11,10 +11,9 @@
 //
 // That array lives in every GPU that loads this part of the library and stays
 // there until the process exits.  All calls on a device share it: it keeps the
-// contents of the previous call, the kernels clear what must start at zero
-// (the dQ accumulator is zeroed by the prep stage on every call), and two calls
-// whose work overlaps on the GPU (different streams, or different host threads
-// without ordering) race on it and give wrong results.
+// contents of the previous call (the prep stage rewrites it on every call), and
+// two calls whose work overlaps on the GPU (different streams, or different
+// host threads without ordering) race on it and give wrong results.
 #include <atomic>
 #include <mutex>
 
@@ -23,8 +22,9 @@
 
 namespace {
 
-// 64 MiB: the fp32 dQ accumulator (4*B*H*N*d bytes) plus D (4*B*H*N bytes),
-// each rounded up to 256 bytes, must fit.
+// 64 MiB: fa_bwd_workspace_size (8 bytes per row, rows padded to whole
+// 128-row tiles) must fit, i.e. up to 2^23 rows; larger sizes return
+// FA_ERR_WORKSPACE.
 constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;
 constexpr int kMaxDevices = 64;
 

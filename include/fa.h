@@ -57,16 +57,16 @@ typedef enum {
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
            int B, int H, int N, int d, float scale, int causal, void* stream);
 
-/* Bytes of device workspace fa_bwd needs for these sizes: an fp32 dQ
- * accumulator [B,H,N,d] and the fp32 row statistic D = rowsum(dO * O) [B,H,N],
- * each rounded up to 256 bytes. */
+/* Bytes of device workspace fa_bwd needs for these sizes: two fp32 row
+ * statistics, D = rowsum(dO * O) and lse * log2(e), each [B*H, N rounded up to
+ * a multiple of 128] and rounded up to 256 bytes (d does not change it). */
 size_t fa_bwd_workspace_size(int B, int H, int N, int d);
 
 /* Backward pass.  Inputs q, k, v, o, lse (as written by fa_fwd) and dout
  * (dL/dO); outputs dq, dk, dv (bf16 [B,H,N,d]).  workspace: caller-owned
  * device memory of at least fa_bwd_workspace_size() bytes, 256-byte aligned;
  * its contents on entry do not matter.  Runs fa_bwd_prep, fa_bwd_main and
- * fa_bwd_finish in order on `stream`.
+ * fa_bwd_dq in order on `stream`.
  * The pages state only that P is recomputed from Q, K and the saved L and that
  * the gradients follow; the formulas used are the softmax Jacobian:
  *   dV = P^T dO, dP = dO V^T, D = rowsum(dO * O), dS = P * (dP - D),
@@ -77,20 +77,25 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
            void* workspace, size_t workspace_bytes, void* stream);
 
 /* The three stages of fa_bwd, exposed so a caller can time or overlap them.
- * prep:   D = rowsum(dO * O) into the workspace and clears the dQ accumulator.
- * main:   per key/value tile, recompute S and P = exp(S - lse), accumulate
- *         dV and dK on chip and add scale * dS K into the dQ accumulator.
- * finish: dq = bf16(dQ accumulator).
- * Arguments mean the same as for fa_bwd; each stage reads what the previous
- * one wrote into the workspace. */
-int fa_bwd_prep(const void* o, const void* dout, int B, int H, int N, int d,
+ * prep: D = rowsum(dO * O) and lse * log2(e) into the workspace.
+ * main: per key/value tile, recompute S and P = exp(S - lse) and accumulate
+ *       dV and dK on chip; writes dk, dv.
+ * dq:   per query tile, recompute S, P and dP = dO V^T and accumulate
+ *       dQ = scale * dS K on chip; writes dq.
+ * main and dq both read D from the workspace (written by prep) and nothing
+ * else of each other, so they may run in either order or concurrently on
+ * two streams once prep has finished.  Arguments mean the same as for
+ * fa_bwd. */
+int fa_bwd_prep(const void* o, const void* dout, const float* lse, int B, int H, int N, int d,
                 void* workspace, size_t workspace_bytes, void* stream);
 int fa_bwd_main(const void* q, const void* k, const void* v, const float* lse,
                 const void* dout, void* dk, void* dv,
                 int B, int H, int N, int d, float scale, int causal,
                 void* workspace, size_t workspace_bytes, void* stream);
-int fa_bwd_finish(void* dq, int B, int H, int N, int d,
-                  void* workspace, size_t workspace_bytes, void* stream);
+int fa_bwd_dq(const void* q, const void* k, const void* v, const float* lse,
+              const void* dout, void* dq,
+              int B, int H, int N, int d, float scale, int causal,
+              void* workspace, size_t workspace_bytes, void* stream);
 
 /* Backward pass for callers that cannot allocate device memory: code that runs
  * where cudaMalloc is unavailable or not allowed, such as inside a custom
@@ -98,10 +103,10 @@ int fa_bwd_finish(void* dq, int B, int H, int N, int d,
  * footprint after start-up, or a plug-in whose host framework owns every
  * allocation.  (The pages have no counterpart: this is a packaging choice of
  * this library.)  Same arguments, results and errors as fa_bwd, minus the workspace: the
- * scratch (fp32 dQ accumulator + D) lives in one fixed 64 MiB array of library
- * device memory, so nothing is allocated.  Sizes whose workspace
- * (fa_bwd_workspace_size) exceeds 64 MiB return FA_ERR_WORKSPACE before any
- * launch.  The first call on a device looks up the array's device address with
+ * scratch (fa_bwd_workspace_size bytes) lives in one fixed 64 MiB array of
+ * library device memory, so nothing is allocated.  Sizes whose workspace
+ * exceeds 64 MiB (more than 2^23 rows B*H*N after rounding N up to a multiple
+ * of 128) return FA_ERR_WORKSPACE before any launch.  The first call on a device looks up the array's device address with
  * that device current; make that first call before any stream capture.  Every
  * call on a device shares the array: calls whose work overlaps on the GPU
  * (other streams, unordered host threads) race on it. */

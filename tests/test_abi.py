@@ -46,9 +46,9 @@ def test_status_strings(lib):
 
 def test_workspace_size(lib):
     B, H, N, d = 2, 3, 100, 64
-    rows = B * H * N
     r256 = lambda x: (x + 255) // 256 * 256
-    assert fa.fa_bwd_workspace_size(B, H, N, d) == r256(rows * d * 4) + r256(rows * 4)
+    npad = B * H * ((N + 127) // 128) * 128
+    assert fa.fa_bwd_workspace_size(B, H, N, d) == 2 * r256(npad * 4)  # D, lse * log2(e)
     assert fa.fa_bwd_workspace_size(0, 1, 1, 64) == 0
 
 
@@ -96,8 +96,10 @@ def test_bwd_argument_errors(lib):
     assert call(15, None) == fa.FA_ERR_WORKSPACE
     assert call(15, FAKE + 16) == fa.FA_ERR_WORKSPACE  # not 256-byte aligned
     assert call(16, ws - 1) == fa.FA_ERR_WORKSPACE
-    assert fa.fa_bwd_prep(None, FAKE, 1, 1, 128, 64, FAKE, ws, None) == fa.FA_ERR_INVALID_ARG
-    assert fa.fa_bwd_finish(None, 1, 1, 128, 64, FAKE, ws, None) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_bwd_prep(None, FAKE, FAKE, 1, 1, 128, 64, FAKE, ws, None) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_bwd_prep(FAKE, FAKE, None, 1, 1, 128, 64, FAKE, ws, None) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_bwd_dq(FAKE, FAKE, FAKE, FAKE, FAKE, None, 1, 1, 128, 64, 0.125, 1, FAKE, ws,
+                        None) == fa.FA_ERR_INVALID_ARG
     assert fa.fa_bwd_main(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 128, 64, 0.125, 1,
                           FAKE, 16, None) == fa.FA_ERR_WORKSPACE
 

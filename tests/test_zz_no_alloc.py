@@ -41,9 +41,10 @@ def test_noalloc_matches_fa_bwd_on_two_calls(d, causal):
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():
-    # 4 * 1 * 64 * 4096 * 128 bytes of dQ accumulator alone is 128 MiB > 64 MiB;
-    # the sizes are rejected before any pointer is touched.
+    # D for 1 * 512 * 32769 > 2^24 rows needs more than 64 MiB (d = 64 keeps the
+    # shape itself under 2^31 elements); the sizes are rejected before any
+    # pointer is touched.
     fake = 0x100000
-    rc = fa.fa_bwd_noalloc(*([fake] * 9), 1, 64, 4096, 128, 0.088, 1,
+    rc = fa.fa_bwd_noalloc(*([fake] * 9), 1, 512, 32769, 64, 0.125, 1,
                            torch.cuda.current_stream().cuda_stream)
     assert rc == fa.FA_ERR_WORKSPACE

@@ -8,49 +8,44 @@ namespace {
 using namespace ptx;
 
 // ---------------------------------------------------------------------------
-// prep: D_i = sum_c dO[i,c] * O[i,c] (fp32) and lse_i * log2(e), one row per
-// warp (16-byte vector loads of O and dO), written for every row of whole
-// 128-row tiles so that the two kernels after it load a tile's 128 values
-// with one bulk copy; padding rows get D = 0 and lse * log2(e) = +inf.
+// prep: D_i = sum_c dO[i,c] * O[i,c] (fp32) and lse_i * log2(e), d/8 threads
+// per row (one 16-byte vector of O and of dO each), written for every row of
+// whole 128-row tiles so that the two kernels after it load a tile's 128
+// values with one bulk copy; padding rows get D = 0 and lse * log2(e) = +inf.
 // ---------------------------------------------------------------------------
 template <int HD>
 __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const BwdArgs a) {
+    constexpr int kTPR = HD / 8;       // threads per row, one 16-byte vector (8 bf16) each
+    constexpr int kRPW = 32 / kTPR;    // rows per warp pass
     const int npad = a.n_kblk * 128;
     const long long rows = static_cast<long long>(a.BH) * npad;
     const int lane = threadIdx.x & 31;
+    const int sub = lane % kTPR;
     const long long warp_global = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
-    constexpr int kVec = HD / 8;  // 16-byte vectors per row (8 bf16 each)
-    for (long long rp = warp_global; rp < rows; rp += nwarps) {
+    for (long long base = warp_global * kRPW; base < rows; base += nwarps * kRPW) {
+        const long long rp = base + lane / kTPR;
         const long long bh = rp / npad;
         const int i = static_cast<int>(rp - bh * npad);
-        if (i >= a.N) {
-            if (lane == 0) {
-                a.delta[rp] = 0.f;
-                a.lse2[rp] = INFINITY;
-            }
-            continue;
-        }
-        const long long r = bh * a.N + i;
+        const bool real = rp < rows && i < a.N;
         float acc = 0.f;
-        const uint4* orow = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.o) + r * HD);
-        const uint4* drow = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.dout) + r * HD);
-        for (int v = lane; v < kVec; v += 32) {
-            const uint4 ov = __ldg(orow + v);
-            const uint4 dv = __ldg(drow + v);
+        if (real) {
+            const long long r = bh * a.N + i;
+            const uint4 ov = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.o) + r * HD) + sub);
+            const uint4 dv = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.dout) + r * HD) + sub);
             const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w};
             const uint32_t dw[4] = {dv.x, dv.y, dv.z, dv.w};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                acc = fmaf(__uint_as_float(ow[i] << 16), __uint_as_float(dw[i] << 16), acc);
-                acc = fmaf(__uint_as_float(ow[i] & 0xffff0000u), __uint_as_float(dw[i] & 0xffff0000u), acc);
+            for (int e = 0; e < 4; ++e) {
+                acc = fmaf(__uint_as_float(ow[e] << 16), __uint_as_float(dw[e] << 16), acc);
+                acc = fmaf(__uint_as_float(ow[e] & 0xffff0000u), __uint_as_float(dw[e] & 0xffff0000u), acc);
             }
         }
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (lane == 0) {
-            a.delta[rp] = acc;
-            a.lse2[rp] = a.lse[r] * 1.4426950408889634f;
+        for (int off = kTPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (sub == 0 && rp < rows) {
+            a.delta[rp] = real ? acc : 0.f;
+            a.lse2[rp] = real ? a.lse[bh * a.N + i] * 1.4426950408889634f : INFINITY;
         }
     }
 }
@@ -482,7 +477,7 @@ int grid_for(long long work_items, int per_block, int max_blocks) {
 
 cudaError_t launch_bwd_prep(int d, const BwdArgs& a, cudaStream_t stream) {
     const long long rows = static_cast<long long>(a.BH) * a.n_kblk * 128;
-    const int grid = grid_for(rows, 8, 152 * 16);
+    const int grid = grid_for(rows, 8 * (32 / (d / 8)), 152 * 16);  // 8 warps, 32/(d/8) rows each
     if (d == 64)
         fa_bwd_prep_kernel<64><<<grid, 256, 0, stream>>>(a);
     else

@@ -10,10 +10,10 @@ using namespace ptx;
 // ---------------------------------------------------------------------------
 // dQ: one CTA per (head, 128-row query tile i), looping over 128-key tiles j
 // (j <= i when causal), with dQ_i accumulated in TMEM for the whole loop:
-//   S    = Q_i K_j^T                  (TMEM, fp32; two buffers)
-//   dP   = dO_i V_j^T                 (TMEM, fp32)
+//   S    = Q_i K_j^T                  (TMEM, fp32)
+//   dP   = dO_i V_j^T                 (TMEM, fp32; two buffers)
 //   P    = exp2(S * scale*log2e - lse_i * log2e)       (recomputed from lse)
-//   dS   = P * (dP - D_i)             (bf16, written over S's columns)
+//   dS   = P * (dP - D_i)             (bf16, written over dP's columns)
 //   dQ_i += dS K_j                    (dS from TMEM, K_j MN-major)
 //   dq_i  = bf16(scale * dQ_i)
 // The same formulas as the dK/dV kernel (the softmax Jacobian), with query
@@ -21,9 +21,12 @@ using namespace ptx;
 // thread needs no exchange with the other thread of its row.  S and dP are
 // recomputed here rather than sending a partial dQ per (i, j) tile out of
 // the SM (see the dK/dV kernel).
-// MMA issue order per key tile: S(j) into buffer j%2, dP(j), dQ(j-1).  S(j+1)
-// only has to wait for dQ(j-1) to have consumed dS(j-1) from the same buffer,
-// so the compute warps find S and dP of the next tile ready.
+// MMA issue order per key tile: S(j), dP(j) into buffer j%2, dQ(j-1).  S(j+1)
+// only waits for the compute warps to have read S(j), and dP(j+1) for dQ(j-1)
+// to have consumed dS(j-1) from the same buffer, so both are ready when the
+// compute warps finish tile j.  K_j is read
+// until dQ(j), V_j only until dP(j), so K and V have rings of their own, K
+// with one more slot.
 // Roles: warp 0 TMA, warp 1 MMA + TMEM allocation, warps 2-5
 // / 6-9 compute for key columns 0-63 / 64-127 of each tile.
 // ---------------------------------------------------------------------------
@@ -35,9 +38,10 @@ template <int HD>
 struct DqCfg {
     static constexpr int kTile = 128 * HD * 2;
     static constexpr int kBoxes = HD / 64;
-    static constexpr int kStages = HD == 128 ? 5 : 10;  // K/V ring slots (K_j, V_j alternate)
-    static constexpr uint32_t kS = 0;     // S / dS buffers at columns 0 and 128
-    static constexpr uint32_t kDP = 256;
+    static constexpr int kKSlots = HD == 128 ? 3 : 6;
+    static constexpr int kVSlots = HD == 128 ? 2 : 4;
+    static constexpr uint32_t kS = 0;
+    static constexpr uint32_t kDP = 128;  // dP / dS buffers at columns 128 and 256
     static constexpr uint32_t kDQ = 384;
     static constexpr uint32_t kTmemCols = 512;
 };
@@ -46,16 +50,19 @@ template <int HD>
 struct alignas(1024) DqSmem {
     uint8_t q[DqCfg<HD>::kTile];
     uint8_t dout[DqCfg<HD>::kTile];
-    uint8_t kv[DqCfg<HD>::kStages][DqCfg<HD>::kTile];
+    uint8_t k[DqCfg<HD>::kKSlots][DqCfg<HD>::kTile];
+    uint8_t v[DqCfg<HD>::kVSlots][DqCfg<HD>::kTile];
     float lse2[128];   // lse * log2(e) per query row (+inf past the end)
     float delta[128];  // D per query row
     uint64_t qd_full;  // Q, dO and their lse * log2(e), D landed
-    uint64_t kv_full[DqCfg<HD>::kStages];
-    uint64_t kv_empty[DqCfg<HD>::kStages];
-    uint64_t s_full[2];    // per S buffer
-    uint64_t dp_full;
-    uint64_t dp_free;      // the compute warps have read dP
-    uint64_t ds_ready[2];  // per S buffer: dS written over it
+    uint64_t k_full[DqCfg<HD>::kKSlots];
+    uint64_t k_empty[DqCfg<HD>::kKSlots];  // committed after dQ(j)
+    uint64_t v_full[DqCfg<HD>::kVSlots];
+    uint64_t v_empty[DqCfg<HD>::kVSlots];  // committed after dP(j)
+    uint64_t s_full;
+    uint64_t s_free;       // the compute warps have read S
+    uint64_t dp_full[2];   // per dP buffer
+    uint64_t ds_ready[2];  // per dP buffer: dS written over it
     uint64_t dq_done;
     uint64_t drain;
     uint32_t tmem_base;
@@ -108,16 +115,20 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
     if (threadIdx.x == 0) {
         sm.abort = 0;
         mbar_init(smem_u32(&sm.qd_full), 1);
-        for (int s = 0; s < Cfg::kStages; ++s) {
-            mbar_init(smem_u32(&sm.kv_full[s]), 1);
-            mbar_init(smem_u32(&sm.kv_empty[s]), 1);
+        for (int s = 0; s < Cfg::kKSlots; ++s) {
+            mbar_init(smem_u32(&sm.k_full[s]), 1);
+            mbar_init(smem_u32(&sm.k_empty[s]), 1);
+        }
+        for (int s = 0; s < Cfg::kVSlots; ++s) {
+            mbar_init(smem_u32(&sm.v_full[s]), 1);
+            mbar_init(smem_u32(&sm.v_empty[s]), 1);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(smem_u32(&sm.s_full[b]), 1);
+            mbar_init(smem_u32(&sm.dp_full[b]), 1);
             mbar_init(smem_u32(&sm.ds_ready[b]), kQCompute);
         }
-        mbar_init(smem_u32(&sm.dp_full), 1);
-        mbar_init(smem_u32(&sm.dp_free), kQCompute);
+        mbar_init(smem_u32(&sm.s_full), 1);
+        mbar_init(smem_u32(&sm.s_free), kQCompute);
         mbar_init(smem_u32(&sm.dq_done), 1);
         mbar_init(smem_u32(&sm.drain), 1);
         fence_mbar_init();
@@ -150,27 +161,38 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             const size_t stat = static_cast<size_t>(bh) * nq * 128 + q0;
             bulk_load(smem_u32(sm.lse2), a.lse2 + stat, 512, qbar);
             bulk_load(smem_u32(sm.delta), a.delta + stat, 512, qbar);
-            // K_j and V_j stream through the ring: K_j is copy 2j, V_j copy 2j + 1.
-            const int n_loads = FA_FAULT_INJECT ? 0 : 2 * n;
+            // K_j then V_j, each into its own ring
+            const int n_loads = FA_FAULT_INJECT ? 0 : n;
             bool ok = true;
-            int issued = 0;
-            for (int idx = 0; idx < n_loads; ++idx) {
-                const int slot = idx % Cfg::kStages;
-                if (!(ok = mbar_wait(smem_u32(&sm.kv_empty[slot]), ((idx / Cfg::kStages) & 1) ^ 1,
+            int issued_k = 0, issued_v = 0;
+            for (int jj = 0; jj < n_loads; ++jj) {
+                const int ks = jj % Cfg::kKSlots, vs = jj % Cfg::kVSlots;
+                if (!(ok = mbar_wait(smem_u32(&sm.k_empty[ks]), ((jj / Cfg::kKSlots) & 1) ^ 1,
                                      kWaitTimeoutNs, abort)))
                     break;
-                const uint32_t bar = smem_u32(&sm.kv_full[slot]);
-                mbar_arrive_expect_tx(bar, Cfg::kTile);
-                const CUtensorMap* map = (idx & 1) ? &tv : &tk;
+                const uint32_t kbar = smem_u32(&sm.k_full[ks]);
+                mbar_arrive_expect_tx(kbar, Cfg::kTile);
                 for (int b = 0; b < Cfg::kBoxes; ++b)
-                    tma_load_3d(smem_u32(sm.kv[slot] + b * kQBox), map, bar, b * 64, (idx >> 1) * 128, bh);
-                ++issued;
+                    tma_load_3d(smem_u32(sm.k[ks] + b * kQBox), &tk, kbar, b * 64, jj * 128, bh);
+                ++issued_k;
+                if (!(ok = mbar_wait(smem_u32(&sm.v_empty[vs]), ((jj / Cfg::kVSlots) & 1) ^ 1,
+                                     kWaitTimeoutNs, abort)))
+                    break;
+                const uint32_t vbar = smem_u32(&sm.v_full[vs]);
+                mbar_arrive_expect_tx(vbar, Cfg::kTile);
+                for (int b = 0; b < Cfg::kBoxes; ++b)
+                    tma_load_3d(smem_u32(sm.v[vs] + b * kQBox), &tv, vbar, b * 64, jj * 128, bh);
+                ++issued_v;
             }
             if (!ok) dq_timeout(a, abort);
             // Let every copy that was issued land before the CTA can exit.
-            for (int slot = 0; slot < Cfg::kStages && slot < issued; ++slot) {
-                const int last = slot + Cfg::kStages * ((issued - 1 - slot) / Cfg::kStages);
-                mbar_wait_drain(smem_u32(&sm.kv_full[slot]), (last / Cfg::kStages) & 1, kWaitTimeoutNs);
+            for (int s = 0; s < Cfg::kKSlots && s < issued_k; ++s) {
+                const int last = s + Cfg::kKSlots * ((issued_k - 1 - s) / Cfg::kKSlots);
+                mbar_wait_drain(smem_u32(&sm.k_full[s]), (last / Cfg::kKSlots) & 1, kWaitTimeoutNs);
+            }
+            for (int s = 0; s < Cfg::kVSlots && s < issued_v; ++s) {
+                const int last = s + Cfg::kVSlots * ((issued_v - 1 - s) / Cfg::kVSlots);
+                mbar_wait_drain(smem_u32(&sm.v_full[s]), (last / Cfg::kVSlots) & 1, kWaitTimeoutNs);
             }
             mbar_wait_drain(qbar, 0, kWaitTimeoutNs);
         }
@@ -180,11 +202,16 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             constexpr uint32_t id_kk = idesc_bf16_f32(128, 128, 0, 0);  // S, dP
             constexpr uint32_t id_dq = idesc_bf16_f32(128, HD, 0, 1);   // dQ: dS from TMEM, K MN-major
             const uint32_t q_addr = smem_u32(sm.q), do_addr = smem_u32(sm.dout);
-            auto wait_kv = [&](int idx) -> bool {
-                return mbar_wait(smem_u32(&sm.kv_full[idx % Cfg::kStages]), (idx / Cfg::kStages) & 1,
+            auto wait_k = [&](int j) -> bool {
+                return mbar_wait(smem_u32(&sm.k_full[j % Cfg::kKSlots]), (j / Cfg::kKSlots) & 1,
                                  kWaitTimeoutNs, abort);
             };
-            auto kv_addr = [&](int idx) -> uint32_t { return smem_u32(sm.kv[idx % Cfg::kStages]); };
+            auto wait_v = [&](int j) -> bool {
+                return mbar_wait(smem_u32(&sm.v_full[j % Cfg::kVSlots]), (j / Cfg::kVSlots) & 1,
+                                 kWaitTimeoutNs, abort);
+            };
+            auto k_addr = [&](int j) -> uint32_t { return smem_u32(sm.k[j % Cfg::kKSlots]); };
+            auto v_addr = [&](int j) -> uint32_t { return smem_u32(sm.v[j % Cfg::kVSlots]); };
             // D[tmem] = A B^T with both operands K-major over the head dimension.
             auto gemm_kk = [&](uint32_t d_col, uint32_t a_addr, uint32_t b_addr) {
 #pragma unroll
@@ -195,38 +222,38 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 }
             };
             // dQ += dS(j) K_j : dS (bf16) from TMEM, keys 0-63 packed at columns
-            // [0,32) of its buffer, keys 64-127 at [64,96); K_j MN-major.
+            // [0,32) of its dP buffer, keys 64-127 at [64,96); K_j MN-major.
             auto issue_dq = [&](int j) -> bool {
                 if (!mbar_wait(smem_u32(&sm.ds_ready[j & 1]), (j >> 1) & 1, kWaitTimeoutNs, abort))
                     return false;
                 tc_fence_after();
-                const uint32_t buf = Cfg::kS + static_cast<uint32_t>(j & 1) * 128;
-                const uint32_t k_addr = kv_addr(2 * j);
+                const uint32_t buf = Cfg::kDP + static_cast<uint32_t>(j & 1) * 128;
+                const uint32_t kj = k_addr(j);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint32_t acol = buf + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
-                    umma_ts(tbase + Cfg::kDQ, tbase + acol, sdesc_sw128(k_addr + kk * 2048, kQBox, 1024),
+                    umma_ts(tbase + Cfg::kDQ, tbase + acol, sdesc_sw128(kj + kk * 2048, kQBox, 1024),
                             id_dq, (j > 0 || kk > 0) ? 1u : 0u);
                 }
-                umma_commit(smem_u32(&sm.kv_empty[(2 * j) % Cfg::kStages]));  // K_j read
+                umma_commit(smem_u32(&sm.k_empty[j % Cfg::kKSlots]));  // K_j read
                 return true;
             };
             bool ok = mbar_wait(smem_u32(&sm.qd_full), 0, kWaitTimeoutNs, abort);
             for (int j = 0; ok && j < n; ++j) {
-                // S(j) into buffer j%2: dS(j-2) there was consumed by dQ(j-2),
-                // issued earlier (the tensor pipe runs one thread's MMAs in order).
-                if (!(ok = wait_kv(2 * j))) break;
-                tc_fence_after();
-                gemm_kk(Cfg::kS + static_cast<uint32_t>(j & 1) * 128, q_addr, kv_addr(2 * j));
-                umma_commit(smem_u32(&sm.s_full[j & 1]));
-                // dP(j): the compute warps have read dP(j-1)
-                if (j > 0 && !(ok = mbar_wait(smem_u32(&sm.dp_free), (j - 1) & 1, kWaitTimeoutNs, abort)))
+                // S(j): the compute warps have read S(j-1)
+                if (j > 0 && !(ok = mbar_wait(smem_u32(&sm.s_free), (j - 1) & 1, kWaitTimeoutNs, abort)))
                     break;
-                if (!(ok = wait_kv(2 * j + 1))) break;
+                if (!(ok = wait_k(j))) break;
                 tc_fence_after();
-                gemm_kk(Cfg::kDP, do_addr, kv_addr(2 * j + 1));
-                umma_commit(smem_u32(&sm.dp_full));
-                umma_commit(smem_u32(&sm.kv_empty[(2 * j + 1) % Cfg::kStages]));  // V_j read
+                gemm_kk(Cfg::kS, q_addr, k_addr(j));
+                umma_commit(smem_u32(&sm.s_full));
+                // dP(j) into buffer j%2: dS(j-2) there was consumed by dQ(j-2),
+                // issued earlier (the tensor pipe runs one thread's MMAs in order).
+                if (!(ok = wait_v(j))) break;
+                tc_fence_after();
+                gemm_kk(Cfg::kDP + static_cast<uint32_t>(j & 1) * 128, do_addr, v_addr(j));
+                umma_commit(smem_u32(&sm.dp_full[j & 1]));
+                umma_commit(smem_u32(&sm.v_empty[j % Cfg::kVSlots]));  // V_j read
                 if (j > 0 && !(ok = issue_dq(j - 1))) break;
             }
             if (ok && n > 0) ok = issue_dq(n - 1);
@@ -248,18 +275,19 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         const float lse2 = ok ? sm.lse2[row] : 0.f;
         const float dval = ok ? sm.delta[row] : 0.f;
         for (int j = 0; ok && j < n; ++j) {
-            const uint32_t buf = Cfg::kS + static_cast<uint32_t>(j & 1) * 128 + half * 64;
-            if (!(ok = mbar_wait_warp(smem_u32(&sm.s_full[j & 1]), (j >> 1) & 1, kWaitTimeoutNs, abort)))
-                break;
+            const uint32_t dbuf = Cfg::kDP + static_cast<uint32_t>(j & 1) * 128 + half * 64;
+            if (!(ok = mbar_wait_warp(smem_u32(&sm.s_full), j & 1, kWaitTimeoutNs, abort))) break;
             tc_fence_after();
             float p[64];
             {
                 uint32_t r0[32], r1[32];
-                tmem_ld32(lane_addr + buf, r0);
-                tmem_ld32(lane_addr + buf + 32, r1);
+                tmem_ld32(lane_addr + Cfg::kS + half * 64, r0);
+                tmem_ld32(lane_addr + Cfg::kS + half * 64 + 32, r1);
                 tmem_wait_ld();
                 reg_fence(r0);
                 reg_fence(r1);
+                tc_fence_before();
+                mbar_arrive(smem_u32(&sm.s_free));
 #pragma unroll
                 for (int c = 0; c < 64; ++c)
                     p[c] = ex2(fmaf(__uint_as_float(c < 32 ? r0[c] : r1[c - 32]), sl2, -lse2));
@@ -271,19 +299,16 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 for (int c = 0; c < 64; ++c)
                     if (kbase + c >= kend) p[c] = 0.f;
             }
-            if (!(ok = mbar_wait_warp(smem_u32(&sm.dp_full), j & 1, kWaitTimeoutNs, abort))) break;
+            if (!(ok = mbar_wait_warp(smem_u32(&sm.dp_full[j & 1]), (j >> 1) & 1, kWaitTimeoutNs, abort)))
+                break;
             tc_fence_after();
             uint32_t pk[32];
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 uint32_t r[32];
-                tmem_ld32(lane_addr + Cfg::kDP + half * 64 + h * 32, r);
+                tmem_ld32(lane_addr + dbuf + h * 32, r);
                 tmem_wait_ld();
                 reg_fence(r);
-                if (h == 1) {
-                    tc_fence_before();
-                    mbar_arrive(smem_u32(&sm.dp_free));
-                }
 #pragma unroll
                 for (int c = 0; c < 16; ++c) {
                     const int e = h * 32 + 2 * c;
@@ -291,8 +316,8 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                                                  p[e + 1] * (__uint_as_float(r[2 * c + 1]) - dval));
                 }
             }
-            // dS over the first 32 columns this thread read: keys 64 half + [0, 64)
-            tmem_st32(lane_addr + buf, pk);
+            // dS over the first 32 of the 64 dP columns this thread read
+            tmem_st32(lane_addr + dbuf, pk);
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(smem_u32(&sm.ds_ready[j & 1]));

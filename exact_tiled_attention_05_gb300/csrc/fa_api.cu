@@ -261,7 +261,10 @@ int fa_bwd_main(const void* q, const void* k, const void* v, const float* lse, c
     if (!aligned16(dk) || !aligned16(dv)) return FA_ERR_MISALIGNED;
     a.dk = dk;
     a.dv = dv;
-    return map_cuda(launch_bwd_dkdv(d, m[0], m[1], m[2], m[3], a, static_cast<cudaStream_t>(stream)));
+    CUtensorMap tdk, tdv;
+    if ((rc = make_map(&tdk, dk, B * H, N, d)) || (rc = make_map(&tdv, dv, B * H, N, d))) return rc;
+    return map_cuda(
+        launch_bwd_dkdv(d, m[0], m[1], m[2], m[3], tdk, tdv, a, static_cast<cudaStream_t>(stream)));
 }
 
 int fa_bwd_dq(const void* q, const void* k, const void* v, const float* lse, const void* dout,

@@ -71,8 +71,12 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const BwdArgs a) {
 // only needs P^T(i) consumed by dV(i), so the compute warps find it ready
 // when they finish dS^T(i).  Q_i is read until dK(i), dO_i only until dV(i),
 // so Q has one more slot than dO.
-// Roles: warp 0 TMA, warp 1 MMA, warp 2 TMEM allocation,
-// warps 4-7 / 8-11 compute for query columns 0-63 / 64-127 of each tile.
+// Epilogue: the compute warps stage bf16 dV and scale * dK, 128-byte
+// swizzled, in two Q slots (free once the last dK has read them) and warp 3
+// writes them out with TMA tile stores (per-thread row stores of a 128-row
+// tile measured ~12 B/clk, the CTA's slowest phase).
+// Roles: warp 0 TMA loads, warp 1 MMA, warp 2 TMEM allocation, warp 3 TMA
+// stores, warps 4-7 / 8-11 compute for query columns 0-63 / 64-127 of each tile.
 // ---------------------------------------------------------------------------
 constexpr int kBThreads = 384;
 constexpr int kBCompute = 256;  // threads of warps 4..11; each arrives on the compute barriers
@@ -104,13 +108,25 @@ struct alignas(1024) BwdSmem {
     uint64_t q_empty[BwdCfg<HD>::kQSlots];   // committed after dK(i)
     uint64_t do_full[BwdCfg<HD>::kDoSlots];  // dO tile and its D landed
     uint64_t do_empty[BwdCfg<HD>::kDoSlots]; // committed after dV(i)
-    uint64_t s_full, dp_full, p_ready, ds_ready, dkdv_done, drain;
+    uint64_t p_ready[2];  // P^T for each thread's queries 0-31, then 32-63
+    uint64_t s_full, dp_full, ds_ready, dkdv_done, drain;
+    uint64_t out_staged;  // every compute thread has staged its dV / dK row
     uint32_t tmem_base;
     int abort;
 };
 
 static_assert(sizeof(BwdSmem<128>) <= 232448, "backward d=128 shared memory exceeds 227 KB");
 static_assert(sizeof(BwdSmem<64>) <= 232448, "backward d=64 shared memory exceeds 227 KB");
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32"
+        " [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(
+            taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
 
 __device__ __forceinline__ void bwd_timeout(const BwdArgs& a, volatile int* abort) {
     *abort = 1;
@@ -121,6 +137,7 @@ template <int HD>
 __global__ void __launch_bounds__(kBThreads, 1)
 fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+                   const __grid_constant__ CUtensorMap tdk, const __grid_constant__ CUtensorMap tdv,
                    const BwdArgs a) {
     using Cfg = BwdCfg<HD>;
     extern __shared__ __align__(1024) uint8_t bsmem_raw[];
@@ -166,10 +183,12 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         }
         mbar_init(smem_u32(&sm.s_full), 1);
         mbar_init(smem_u32(&sm.dp_full), 1);
-        mbar_init(smem_u32(&sm.p_ready), kBCompute);
+        mbar_init(smem_u32(&sm.p_ready[0]), kBCompute);
+        mbar_init(smem_u32(&sm.p_ready[1]), kBCompute);
         mbar_init(smem_u32(&sm.ds_ready), kBCompute);
         mbar_init(smem_u32(&sm.dkdv_done), 1);
         mbar_init(smem_u32(&sm.drain), 1);
+        mbar_init(smem_u32(&sm.out_staged), kBCompute);
         fence_mbar_init();
     }
     if (warp == 2) {
@@ -285,10 +304,23 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                 tc_fence_after();
                 gemm_kk(Cfg::kDP, v_addr, do_addr);
                 umma_commit(smem_u32(&sm.dp_full));
-                if (!(ok = mbar_wait(smem_u32(&sm.p_ready), it & 1, kWaitTimeoutNs, abort))) break;
-                tc_fence_after();
-                gemm_tmem_a(Cfg::kDV, Cfg::kS, do_addr, it > 0);  // dV += P^T dO
-                umma_commit(smem_u32(&sm.do_empty[ds]));           // dO_i read
+                // dV += P^T dO in two parts: queries {0-31, 64-95} (k-steps 0, 1, 4, 5),
+                // each thread's first half of P^T, then {32-63, 96-127}
+                for (int part = 0; ok && part < 2; ++part) {
+                    if (!(ok = mbar_wait(smem_u32(&sm.p_ready[part]), it & 1, kWaitTimeoutNs, abort)))
+                        break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int x = 0; x < 4; ++x) {
+                        const int kk = (x >> 1) * 4 + part * 2 + (x & 1);
+                        const uint32_t col = Cfg::kS + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
+                        umma_ts(tbase + Cfg::kDV, tbase + col,
+                                sdesc_sw128(do_addr + kk * 2048, kBBox, 1024), id_kmn,
+                                (it > 0 || part > 0 || x > 0) ? 1u : 0u);
+                    }
+                }
+                if (!ok) break;
+                umma_commit(smem_u32(&sm.do_empty[ds]));  // dO_i read
                 // S^T(i+1) over P^T(i): dV(i) was issued before it.
                 if (it + 1 < niter) {
                     const int qs1 = (it + 1) % Cfg::kQSlots;
@@ -310,6 +342,22 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             umma_commit(smem_u32(&sm.drain));
             mbar_wait_drain(smem_u32(&sm.drain), 0, kWaitTimeoutNs);
         }
+    } else if (warp == 3) {
+        // ===================== dK / dV stores =====================
+        if (elect_one()) {
+            tma_prefetch_desc(&tdk);
+            tma_prefetch_desc(&tdv);
+            if (mbar_wait(smem_u32(&sm.out_staged), 0, kWaitTimeoutNs, abort)) {
+                for (int b = 0; b < Cfg::kBoxes; ++b) {
+                    tma_store_3d(&tdv, smem_u32(sm.q[0]) + b * kBBox, b * 64, j * 128, bh);
+                    tma_store_3d(&tdk, smem_u32(sm.q[1]) + b * kBBox, b * 64, j * 128, bh);
+                }
+                bulk_commit_group();
+                bulk_wait_group0();  // written out before the CTA leaves
+            } else {
+                bwd_timeout(a, abort);
+            }
+        }
     } else if (warp >= 4) {
         // ===================== compute =====================
         const int wg = (warp - 4) >> 2;  // query-column half of S^T / dP^T, and column half of dK/dV
@@ -328,6 +376,9 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                                 abort);
             if (!ok) break;
             tc_fence_after();
+            // P^T in two halves of this thread's 64 query columns; each half is
+            // signalled as soon as it is stored so dV starts on it (the second
+            // half's exponentials overlap the first half's MMAs).
             float p[64];
             {
                 uint32_t r0[32], r1[32];
@@ -337,38 +388,32 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                 reg_fence(r0);
                 reg_fence(r1);
                 const uint32_t lse_addr = smem_u32(&sm.lse2[qs][wg * 64]);
+                const bool diag = a.causal && i == j;
 #pragma unroll
-                for (int c4 = 0; c4 < 16; ++c4) {
-                    const float4 l4 = ld_shared_f4(lse_addr + c4 * 16);
-                    const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+                for (int part = 0; part < 2; ++part) {
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int c = c4 * 4 + e;
-                        const float sv = __uint_as_float(c < 32 ? r0[c] : r1[c - 32]);
-                        p[c] = ex2(fmaf(sv, sl2, -lv[e]));
+                    for (int c4 = 0; c4 < 8; ++c4) {
+                        const float4 l4 = ld_shared_f4(lse_addr + (part * 8 + c4) * 16);
+                        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int c = part * 32 + c4 * 4 + e;
+                            const float sv = __uint_as_float(part == 0 ? r0[c] : r1[c - 32]);
+                            p[c] = ex2(fmaf(sv, sl2, -lv[e]));
+                            // rows past the end, and on the diagonal tile queries before the key
+                            if (!row_valid || (diag && wg * 64 + c < row)) p[c] = 0.f;
+                        }
                     }
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) pk[c] = pack_bf16x2(p[part * 32 + 2 * c], p[part * 32 + 2 * c + 1]);
+                    // P^T over columns this thread read itself
+                    tmem_st16(lane_addr + Cfg::kS + wg * 64 + part * 16, pk);
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(smem_u32(&sm.p_ready[part]));
                 }
             }
-            if (!row_valid) {
-#pragma unroll
-                for (int c = 0; c < 64; ++c) p[c] = 0.f;
-            } else if (a.causal && i == j) {
-                // diagonal tile: query q sees key k only when q >= k
-                const int qbase = wg * 64;
-#pragma unroll
-                for (int c = 0; c < 64; ++c)
-                    if (qbase + c < row) p[c] = 0.f;
-            }
-            {
-                // P^T over the first 32 of the 64 columns this thread read
-                uint32_t pk[32];
-#pragma unroll
-                for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(p[2 * c], p[2 * c + 1]);
-                tmem_st32(lane_addr + Cfg::kS + wg * 64, pk);
-                tmem_wait_st();
-            }
-            tc_fence_before();
-            mbar_arrive(smem_u32(&sm.p_ready));
 
             ok = mbar_wait_warp(smem_u32(&sm.dp_full), it & 1, kWaitTimeoutNs, abort) &&
                  mbar_wait_warp(smem_u32(&sm.do_full[ds]), (it / Cfg::kDoSlots) & 1, kWaitTimeoutNs,
@@ -409,16 +454,19 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             ok = mbar_wait_warp(smem_u32(&sm.dkdv_done), 0, kWaitTimeoutNs, abort);
             if (ok) {
                 tc_fence_after();
+                // this thread's row of columns [wg * d/2, (wg + 1) * d/2) of dV (into
+                // q[0]) and dK (into q[1]): 64-column boxes of 128-byte rows, 16-byte
+                // chunk c of row r at position c ^ (r % 8)
                 constexpr int kHalf = HD / 2;
-                const bool store = kglob < N;
-                const size_t off = (static_cast<size_t>(bh) * N + kglob) * HD + wg * kHalf;
-                uint8_t* dv_dst = static_cast<uint8_t*>(a.dv) + off * 2;
-                uint8_t* dk_dst = static_cast<uint8_t*>(a.dk) + off * 2;
+                const int col0 = wg * kHalf;
+                const uint32_t row_off = static_cast<uint32_t>((col0 / 64) * kBBox + row * 128);
+                const uint32_t dv_row = smem_u32(sm.q[0]) + row_off;
+                const uint32_t dk_row = smem_u32(sm.q[1]) + row_off;
 #pragma unroll 1
                 for (int c = 0; c < kHalf; c += 32) {
                     uint32_t rv[32], rk[32];
-                    tmem_ld32(lane_addr + Cfg::kDV + wg * kHalf + c, rv);
-                    tmem_ld32(lane_addr + Cfg::kDK + wg * kHalf + c, rk);
+                    tmem_ld32(lane_addr + Cfg::kDV + col0 + c, rv);
+                    tmem_ld32(lane_addr + Cfg::kDK + col0 + c, rk);
                     tmem_wait_ld();
                     reg_fence(rv);
                     reg_fence(rk);
@@ -429,16 +477,16 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                         pkk[e] = pack_bf16x2(a.scale * __uint_as_float(rk[2 * e]),
                                              a.scale * __uint_as_float(rk[2 * e + 1]));
                     }
-                    if (store) {
 #pragma unroll
-                        for (int v4 = 0; v4 < 4; ++v4) {
-                            st_global_v4(dv_dst + c * 2 + v4 * 16, pv[4 * v4], pv[4 * v4 + 1],
-                                         pv[4 * v4 + 2], pv[4 * v4 + 3]);
-                            st_global_v4(dk_dst + c * 2 + v4 * 16, pkk[4 * v4], pkk[4 * v4 + 1],
-                                         pkk[4 * v4 + 2], pkk[4 * v4 + 3]);
-                        }
+                    for (int m = 0; m < 4; ++m) {
+                        const int chunk = ((col0 % 64) + c) / 8 + m;
+                        const uint32_t sw = static_cast<uint32_t>((chunk ^ (row & 7)) << 4);
+                        st_shared_v4(dv_row + sw, pv[4 * m], pv[4 * m + 1], pv[4 * m + 2], pv[4 * m + 3]);
+                        st_shared_v4(dk_row + sw, pkk[4 * m], pkk[4 * m + 1], pkk[4 * m + 2], pkk[4 * m + 3]);
                     }
                 }
+                fence_proxy_async_smem();
+                mbar_arrive(smem_u32(&sm.out_staged));
             } else if (lane == 0) {
                 bwd_timeout(a, abort);
             }
@@ -455,14 +503,15 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
 
 template <int HD>
 cudaError_t launch_bwd_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                              const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t stream) {
+                              const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
+                              const BwdArgs& a, cudaStream_t stream) {
     const size_t smem = sizeof(BwdSmem<HD>);
     cudaError_t e = cudaFuncSetAttribute(fa_bwd_dkdv_kernel<HD>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     const unsigned grid = static_cast<unsigned>(a.n_kblk) * static_cast<unsigned>(a.BH);
-    fa_bwd_dkdv_kernel<HD><<<grid, kBThreads, smem, stream>>>(tq, tk, tv, tdo, a);
+    fa_bwd_dkdv_kernel<HD><<<grid, kBThreads, smem, stream>>>(tq, tk, tv, tdo, tdk, tdv, a);
     return cudaGetLastError();
 }
 
@@ -486,10 +535,10 @@ cudaError_t launch_bwd_prep(int d, const BwdArgs& a, cudaStream_t stream) {
 }
 
 cudaError_t launch_bwd_dkdv(int d, const CUtensorMap& tq, const CUtensorMap& tk,
-                            const CUtensorMap& tv, const CUtensorMap& tdo, const BwdArgs& a,
-                            cudaStream_t stream) {
-    if (d == 64) return launch_bwd_dkdv_t<64>(tq, tk, tv, tdo, a, stream);
-    return launch_bwd_dkdv_t<128>(tq, tk, tv, tdo, a, stream);
+                            const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdk,
+                            const CUtensorMap& tdv, const BwdArgs& a, cudaStream_t stream) {
+    if (d == 64) return launch_bwd_dkdv_t<64>(tq, tk, tv, tdo, tdk, tdv, a, stream);
+    return launch_bwd_dkdv_t<128>(tq, tk, tv, tdo, tdk, tdv, a, stream);
 }
 
 }  // namespace fa

@@ -278,7 +278,9 @@ int fa_bwd_dq(const void* q, const void* k, const void* v, const float* lse, con
     if (rc) return rc;
     if (!aligned16(dq)) return FA_ERR_MISALIGNED;
     a.dq = dq;
-    return map_cuda(launch_bwd_dq(d, m[0], m[1], m[2], m[3], a, static_cast<cudaStream_t>(stream)));
+    CUtensorMap tdq;
+    if ((rc = make_map(&tdq, dq, B * H, N, d))) return rc;
+    return map_cuda(launch_bwd_dq(d, m[0], m[1], m[2], m[3], tdq, a, static_cast<cudaStream_t>(stream)));
 }
 
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,

@@ -27,7 +27,10 @@ using namespace ptx;
 // compute warps finish tile j.  K_j is read
 // until dQ(j), V_j only until dP(j), so K and V have rings of their own, K
 // with one more slot.
-// Roles: warp 0 TMA, warp 1 MMA + TMEM allocation, warps 2-5
+// Epilogue: the compute warps stage bf16 scale * dQ, 128-byte swizzled, in K
+// slot 0 (free once the last dQ has read it) and warp 0 writes the tile with
+// TMA stores (per-thread row stores are the slow path, see the dK/dV kernel).
+// Roles: warp 0 TMA loads and stores, warp 1 MMA + TMEM allocation, warps 2-5
 // / 6-9 compute for key columns 0-63 / 64-127 of each tile.
 // ---------------------------------------------------------------------------
 constexpr int kQThreads = 320;
@@ -65,6 +68,7 @@ struct alignas(1024) DqSmem {
     uint64_t ds_ready[2];  // per dP buffer: dS written over it
     uint64_t dq_done;
     uint64_t drain;
+    uint64_t out_staged;  // every compute thread has staged its dQ row
     uint32_t tmem_base;
     int abort;
 };
@@ -81,7 +85,7 @@ template <int HD>
 __global__ void __launch_bounds__(kQThreads, 1)
 fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                  const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
-                 const BwdArgs a) {
+                 const __grid_constant__ CUtensorMap tdq, const BwdArgs a) {
     using Cfg = DqCfg<HD>;
     extern __shared__ __align__(1024) uint8_t qsmem_raw[];
     if ((smem_u32(qsmem_raw) & 1023u) != 0u) {  // the swizzled layouts need 1 KB alignment
@@ -131,6 +135,7 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         mbar_init(smem_u32(&sm.s_free), kQCompute);
         mbar_init(smem_u32(&sm.dq_done), 1);
         mbar_init(smem_u32(&sm.drain), 1);
+        mbar_init(smem_u32(&sm.out_staged), kQCompute);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -195,6 +200,16 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 mbar_wait_drain(smem_u32(&sm.v_full[s]), (last / Cfg::kVSlots) & 1, kWaitTimeoutNs);
             }
             mbar_wait_drain(qbar, 0, kWaitTimeoutNs);
+            // the staged dQ tile
+            tma_prefetch_desc(&tdq);
+            if (ok && mbar_wait(smem_u32(&sm.out_staged), 0, kWaitTimeoutNs, abort)) {
+                for (int b = 0; b < Cfg::kBoxes; ++b)
+                    tma_store_3d(&tdq, smem_u32(sm.k[0]) + b * kQBox, b * 64, q0, bh);
+                bulk_commit_group();
+                bulk_wait_group0();  // written out before the CTA leaves
+            } else {
+                dq_timeout(a, abort);
+            }
         }
     } else if (warp == 1) {
         // ===================== MMA issuer =====================
@@ -328,14 +343,16 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             ok = mbar_wait_warp(smem_u32(&sm.dq_done), 0, kWaitTimeoutNs, abort);
             if (ok) {
                 tc_fence_after();
+                // this thread's row of columns [half * d/2, (half + 1) * d/2) of dQ into
+                // K slot 0: 64-column boxes of 128-byte rows, 16-byte chunk c of row r
+                // at position c ^ (r % 8)
                 constexpr int kHalf = HD / 2;
-                const bool store = qi < N;
-                const size_t off = (static_cast<size_t>(bh) * N + qi) * HD + half * kHalf;
-                uint8_t* dst = static_cast<uint8_t*>(a.dq) + off * 2;
+                const int col0 = half * kHalf;
+                const uint32_t dst = smem_u32(sm.k[0]) + static_cast<uint32_t>((col0 / 64) * kQBox + row * 128);
 #pragma unroll 1
                 for (int c = 0; c < kHalf; c += 32) {
                     uint32_t r[32];
-                    tmem_ld32(lane_addr + Cfg::kDQ + half * kHalf + c, r);
+                    tmem_ld32(lane_addr + Cfg::kDQ + col0 + c, r);
                     tmem_wait_ld();
                     reg_fence(r);
                     uint32_t w[16];
@@ -343,13 +360,15 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                     for (int e = 0; e < 16; ++e)
                         w[e] = pack_bf16x2(a.scale * __uint_as_float(r[2 * e]),
                                            a.scale * __uint_as_float(r[2 * e + 1]));
-                    if (store) {
 #pragma unroll
-                        for (int v4 = 0; v4 < 4; ++v4)
-                            st_global_v4(dst + c * 2 + v4 * 16, w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2],
-                                         w[4 * v4 + 3]);
+                    for (int m = 0; m < 4; ++m) {
+                        const int chunk = ((col0 % 64) + c) / 8 + m;
+                        st_shared_v4(dst + static_cast<uint32_t>((chunk ^ (row & 7)) << 4), w[4 * m],
+                                     w[4 * m + 1], w[4 * m + 2], w[4 * m + 3]);
                     }
                 }
+                fence_proxy_async_smem();
+                mbar_arrive(smem_u32(&sm.out_staged));
             } else if (lane == 0) {
                 dq_timeout(a, abort);
             }
@@ -366,24 +385,25 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
 
 template <int HD>
 cudaError_t launch_bwd_dq_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t stream) {
+                            const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a,
+                            cudaStream_t stream) {
     const size_t smem = sizeof(DqSmem<HD>);
     cudaError_t e = cudaFuncSetAttribute(fa_bwd_dq_kernel<HD>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     const unsigned grid = static_cast<unsigned>(a.n_kblk) * static_cast<unsigned>(a.BH);
-    fa_bwd_dq_kernel<HD><<<grid, kQThreads, smem, stream>>>(tq, tk, tv, tdo, a);
+    fa_bwd_dq_kernel<HD><<<grid, kQThreads, smem, stream>>>(tq, tk, tv, tdo, tdq, a);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_bwd_dq(int d, const CUtensorMap& tq, const CUtensorMap& tk,
-                          const CUtensorMap& tv, const CUtensorMap& tdo, const BwdArgs& a,
-                          cudaStream_t stream) {
-    if (d == 64) return launch_bwd_dq_t<64>(tq, tk, tv, tdo, a, stream);
-    return launch_bwd_dq_t<128>(tq, tk, tv, tdo, a, stream);
+                          const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
+                          const BwdArgs& a, cudaStream_t stream) {
+    if (d == 64) return launch_bwd_dq_t<64>(tq, tk, tv, tdo, tdq, a, stream);
+    return launch_bwd_dq_t<128>(tq, tk, tv, tdo, tdq, a, stream);
 }
 
 }  // namespace fa

@@ -85,7 +85,7 @@ cudaError_t launch_bwd_dkdv(int d, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdk,
                             const CUtensorMap& tdv, const BwdArgs& args, cudaStream_t stream);
 cudaError_t launch_bwd_dq(int d, const CUtensorMap& tq, const CUtensorMap& tk,
-                          const CUtensorMap& tv, const CUtensorMap& tdo, const BwdArgs& args,
-                          cudaStream_t stream);
+                          const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
+                          const BwdArgs& args, cudaStream_t stream);
 
 }  // namespace fa

@@ -213,9 +213,9 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
     FwdArgs a{};
     if ((rc = device_ready(&a.status))) return rc;
     const int BH = B * H;
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to;
     if ((rc = make_map(&tq, q, BH, N, d)) || (rc = make_map(&tk, k, BH, N, d)) ||
-        (rc = make_map(&tv, v, BH, N, d)))
+        (rc = make_map(&tv, v, BH, N, d)) || (rc = make_map(&to, o, BH, N, d)))
         return rc;
     a.o = o;
     a.lse = lse;
@@ -227,7 +227,7 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
     a.group = clampi(floor_pow2(clampi((2 * current_sms()) / a.n_qblk, 1, 1 << 20)), 1, BH);
     a.causal = causal;
     a.scale_log2 = scale * 1.4426950408889634f;
-    return map_cuda(launch_fwd(d, tq, tk, tv, a, static_cast<cudaStream_t>(stream)));
+    return map_cuda(launch_fwd(d, tq, tk, tv, to, a, static_cast<cudaStream_t>(stream)));
 }
 
 size_t fa_bwd_workspace_size(int B, int H, int N, int d) {

@@ -70,6 +70,10 @@ constexpr int kPParts = 2;
 // 8i + 2(L%4) + {0, 1} of the first row, then the same of the second.
 // 16x128b: per repetition i, registers 2i, 2i+1 are column 4i + L%4 of the
 // first and of the second row.
+__device__ __forceinline__ void st_shared_b32(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld_16x256b_x8(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.16x256b.x8.b32"
@@ -133,6 +137,7 @@ struct alignas(1024) FwdSmem {
     uint64_t s_full[2];
     uint64_t p_full[2][kPParts];  // [tile][part of P]
     uint64_t o_done[2];
+    uint64_t out_staged[2];  // per tile: every softmax thread has staged its O rows
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
@@ -149,7 +154,8 @@ __device__ __forceinline__ void record_timeout(FwdArgs const& a, volatile int* a
 template <int HD>
 __global__ void __launch_bounds__(kThreads, 1)
 fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-              const __grid_constant__ CUtensorMap tv, const FwdArgs args) {
+              const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
+              const FwdArgs args) {
     using Cfg = FwdCfg<HD>;
     extern __shared__ uint8_t smem_raw[];
     FwdSmem<HD>& sm = *reinterpret_cast<FwdSmem<HD>*>(
@@ -206,6 +212,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
             for (int part = 0; part < kPParts; ++part)
                 mbar_init(smem_u32(&sm.p_full[t][part]), kSoftmaxPerTile);
             mbar_init(smem_u32(&sm.o_done[t]), 1);
+            mbar_init(smem_u32(&sm.out_staged[t]), kSoftmaxPerTile);
         }
         mbar_init(smem_u32(&sm.drain), 1);
         fence_mbar_init();
@@ -234,12 +241,14 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                     tma_load_3d(smem_u32(sm.q[t] + b * kBoxBytes), &tq, qbar, b * 64, q0[t], bh);
             }
             int issued = 0;
+            bool ok = true;
             const int n_loads = FA_FAULT_INJECT ? 0 : 2 * nmax;
             for (int idx = 0; idx < n_loads; ++idx) {
                 const int slot = idx % Cfg::kStages;
                 const uint32_t ph = (idx / Cfg::kStages) & 1;
                 if (!mbar_wait(smem_u32(&sm.kv_empty[slot]), ph ^ 1, kWaitTimeoutNs, abort)) {
                     record_timeout(args, abort);
+                    ok = false;
                     break;
                 }
                 const uint32_t fbar = smem_u32(&sm.kv_full[slot]);
@@ -257,6 +266,19 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                                 kWaitTimeoutNs);
             }
             mbar_wait_drain(qbar, 0, kWaitTimeoutNs);
+            // O of each tile, staged by the softmax warps over the tile's Q buffer
+            tma_prefetch_desc(&to);
+            for (int t = 0; ok && t < 2; ++t) {
+                if (nkv[t] == 0) continue;
+                if (!(ok = mbar_wait(smem_u32(&sm.out_staged[t]), 0, kWaitTimeoutNs, abort))) {
+                    record_timeout(args, abort);
+                    break;
+                }
+                for (int b = 0; b < Cfg::kBoxes; ++b)
+                    tma_store_3d(&to, smem_u32(sm.q[t]) + b * kBoxBytes, b * 64, q0[t], bh);
+            }
+            bulk_commit_group();
+            bulk_wait_group0();  // written out before the CTA leaves
         }
     } else if (warp == 1) {
         // ===================== MMA issuer =====================
@@ -541,9 +563,11 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                 tc_fence_after();
                 const float invA = 1.f / (sA + lcA), invB = 1.f / (sB + lcB);
                 const bool storeA = qA < N, storeB = qB < N;
-                uint8_t* oA = reinterpret_cast<uint8_t*>(args.o) +
-                              ((static_cast<size_t>(bh) * N + qA) * HD + 2 * cq) * 2;
-                uint8_t* oB = oA + static_cast<size_t>(8) * HD * 2;
+                // O rows rA and rB into the tile's Q buffer (free: the tile's last
+                // S MMA finished before its last P V), as 64-column boxes of
+                // 128-byte rows; column 8i + 2cq is 16-byte chunk i % 8 of box i / 8,
+                // at position (i % 8) ^ (row % 8), bytes 4cq.. (rB % 8 == rA % 8)
+                const uint32_t qbuf = smem_u32(sm.q[t]);
 #pragma unroll
                 for (int c = 0; c < HD / 32; ++c) {
                     uint32_t r[16];
@@ -556,11 +580,15 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                                                         __uint_as_float(r[4 * i + 1]) * invA);
                         const uint32_t wb = pack_bf16x2(__uint_as_float(r[4 * i + 2]) * invB,
                                                         __uint_as_float(r[4 * i + 3]) * invB);
-                        const int col = c * 32 + 8 * i;  // + 2cq, folded into oA / oB
-                        if (storeA) *reinterpret_cast<uint32_t*>(oA + col * 2) = wa;
-                        if (storeB) *reinterpret_cast<uint32_t*>(oB + col * 2) = wb;
+                        const int ii = c * 4 + i;
+                        const uint32_t off = static_cast<uint32_t>(
+                            (ii / 8) * kBoxBytes + (((ii % 8) ^ (rA & 7)) << 4) + 4 * cq);
+                        st_shared_b32(qbuf + off + static_cast<uint32_t>(rA * 128), wa);
+                        st_shared_b32(qbuf + off + static_cast<uint32_t>((rA + 8) * 128), wb);
                     }
                 }
+                fence_proxy_async_smem();
+                mbar_arrive(smem_u32(&sm.out_staged[t]));
                 if (cq == 0) {
                     if (storeA)
                         args.lse[static_cast<size_t>(bh) * N + qA] =
@@ -585,23 +613,23 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
 
 template <int HD>
 cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                         const FwdArgs& args, cudaStream_t stream) {
+                         const CUtensorMap& to, const FwdArgs& args, cudaStream_t stream) {
     const size_t smem = sizeof(FwdSmem<HD>) + 1024;
     cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<HD>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     const unsigned grid = static_cast<unsigned>(args.n_qblk) * static_cast<unsigned>(args.BH);
-    fa_fwd_kernel<HD><<<grid, kThreads, smem, stream>>>(tq, tk, tv, args);
+    fa_fwd_kernel<HD><<<grid, kThreads, smem, stream>>>(tq, tk, tv, to, args);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const FwdArgs& args, cudaStream_t stream) {
-    if (d == 64) return launch_fwd_t<64>(tq, tk, tv, args, stream);
-    return launch_fwd_t<128>(tq, tk, tv, args, stream);
+                       const CUtensorMap& to, const FwdArgs& args, cudaStream_t stream) {
+    if (d == 64) return launch_fwd_t<64>(tq, tk, tv, to, args, stream);
+    return launch_fwd_t<128>(tq, tk, tv, to, args, stream);
 }
 
 }  // namespace fa

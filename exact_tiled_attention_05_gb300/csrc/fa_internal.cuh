@@ -79,7 +79,7 @@ struct TensorMaps3 {
 
 // Launchers (defined in the kernel translation units).  Return a cudaError_t.
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const FwdArgs& args, cudaStream_t stream);
+                       const CUtensorMap& to, const FwdArgs& args, cudaStream_t stream);
 cudaError_t launch_bwd_prep(int d, const BwdArgs& args, cudaStream_t stream);
 cudaError_t launch_bwd_dkdv(int d, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdk,

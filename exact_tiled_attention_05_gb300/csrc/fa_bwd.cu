@@ -17,35 +17,49 @@ template <int HD>
 __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const BwdArgs a) {
     constexpr int kTPR = HD / 8;       // threads per row, one 16-byte vector (8 bf16) each
     constexpr int kRPW = 32 / kTPR;    // rows per warp pass
+    constexpr int kUnroll = 4;         // passes whose loads are in flight together
     const int npad = a.n_kblk * 128;
     const long long rows = static_cast<long long>(a.BH) * npad;
     const int lane = threadIdx.x & 31;
     const int sub = lane % kTPR;
     const long long warp_global = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
-    for (long long base = warp_global * kRPW; base < rows; base += nwarps * kRPW) {
-        const long long rp = base + lane / kTPR;
-        const long long bh = rp / npad;
-        const int i = static_cast<int>(rp - bh * npad);
-        const bool real = rp < rows && i < a.N;
-        float acc = 0.f;
-        if (real) {
+    for (long long base = warp_global * kRPW * kUnroll; base < rows; base += nwarps * kRPW * kUnroll) {
+        uint4 ov[kUnroll], dv[kUnroll];
+        float lv[kUnroll];
+        long long rp[kUnroll];
+        bool real[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            rp[u] = base + u * kRPW + lane / kTPR;
+            const long long bh = rp[u] / npad;
+            const int i = static_cast<int>(rp[u] - bh * npad);
+            real[u] = rp[u] < rows && i < a.N;
             const long long r = bh * a.N + i;
-            const uint4 ov = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.o) + r * HD) + sub);
-            const uint4 dv = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.dout) + r * HD) + sub);
-            const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w};
-            const uint32_t dw[4] = {dv.x, dv.y, dv.z, dv.w};
+            ov[u] = dv[u] = make_uint4(0u, 0u, 0u, 0u);
+            lv[u] = INFINITY;
+            if (real[u]) {
+                ov[u] = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.o) + r * HD) + sub);
+                dv[u] = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.dout) + r * HD) + sub);
+                if (sub == 0) lv[u] = __ldg(a.lse + r) * 1.4426950408889634f;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const uint32_t ow[4] = {ov[u].x, ov[u].y, ov[u].z, ov[u].w};
+            const uint32_t dw[4] = {dv[u].x, dv[u].y, dv[u].z, dv[u].w};
+            float acc = 0.f;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 acc = fmaf(__uint_as_float(ow[e] << 16), __uint_as_float(dw[e] << 16), acc);
                 acc = fmaf(__uint_as_float(ow[e] & 0xffff0000u), __uint_as_float(dw[e] & 0xffff0000u), acc);
             }
-        }
 #pragma unroll
-        for (int off = kTPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (sub == 0 && rp < rows) {
-            a.delta[rp] = real ? acc : 0.f;
-            a.lse2[rp] = real ? a.lse[bh * a.N + i] * 1.4426950408889634f : INFINITY;
+            for (int off = kTPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+            if (sub == 0 && rp[u] < rows) {
+                a.delta[rp[u]] = real[u] ? acc : 0.f;
+                a.lse2[rp[u]] = lv[u];  // +inf for padding rows
+            }
         }
     }
 }
@@ -526,7 +540,7 @@ int grid_for(long long work_items, int per_block, int max_blocks) {
 
 cudaError_t launch_bwd_prep(int d, const BwdArgs& a, cudaStream_t stream) {
     const long long rows = static_cast<long long>(a.BH) * a.n_kblk * 128;
-    const int grid = grid_for(rows, 8 * (32 / (d / 8)), 152 * 16);  // 8 warps, 32/(d/8) rows each
+    const int grid = grid_for(rows, 8 * (32 / (d / 8)) * 4, 152 * 8);  // 8 warps x 4 passes of 32/(d/8) rows
     if (d == 64)
         fa_bwd_prep_kernel<64><<<grid, 256, 0, stream>>>(a);
     else

@@ -25,8 +25,12 @@ FA_ERR_DEVICE_TIMEOUT = 6
 
 EXPORTED = (
     "fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_bwd_prep", "fa_bwd_main",
-    "fa_bwd_dq", "fa_bwd_noalloc", "fa_sync_status", "fa_status_string", "fa_version",
+    "fa_bwd_dq", "fa_bwd_noalloc", "fa_fp8_workspace_size", "fa_fp8_quantize", "fa_fwd_fp8",
+    "fa_sync_status", "fa_status_string", "fa_version",
 )
+
+FA_FP8_ROTATE = 1
+FA_FP8_PER_TENSOR = 2
 
 _lib = None
 
@@ -56,6 +60,9 @@ def load_library(path: str = LIB_PATH):
         "fa_bwd_main": ([P, P, P, P, P, P, P, I, I, I, I, F, I, P, Z, P], I),
         "fa_bwd_dq": ([P, P, P, P, P, P, I, I, I, I, F, I, P, Z, P], I),
         "fa_bwd_noalloc": ([P, P, P, P, P, P, P, P, P, I, I, I, I, F, I, P], I),
+        "fa_fp8_workspace_size": ([I, I, I, I], Z),
+        "fa_fp8_quantize": ([P, P, P, I, I, I, I, P, I, P, Z, P], I),
+        "fa_fwd_fp8": ([P, Z, P, P, I, I, I, I, F, I, P], I),
         "fa_sync_status": ([P], I),
         "fa_status_string": ([I], ctypes.c_char_p),
         "fa_version": ([], I),
@@ -104,6 +111,19 @@ def fa_bwd_noalloc(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, causal,
     device memory: the scratch is a fixed 64 MiB array inside the library."""
     return load_library().fa_bwd_noalloc(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale,
                                          causal, stream)
+
+
+def fa_fp8_workspace_size(B, H, N, d):
+    return load_library().fa_fp8_workspace_size(B, H, N, d)
+
+
+def fa_fp8_quantize(q, k, v, B, H, N, d, signs, flags, ws, ws_bytes, stream):
+    """signs: a ctypes array of four c_uint32 (or None without FA_FP8_ROTATE)."""
+    return load_library().fa_fp8_quantize(q, k, v, B, H, N, d, signs, flags, ws, ws_bytes, stream)
+
+
+def fa_fwd_fp8(ws, ws_bytes, o, lse, B, H, N, d, scale, causal, stream):
+    return load_library().fa_fwd_fp8(ws, ws_bytes, o, lse, B, H, N, d, scale, causal, stream)
 
 
 def fa_sync_status(stream):
@@ -211,6 +231,105 @@ def backward(q, k, v, o, lse, dout, scale=None, causal=False, dq=None, dk=None, 
 def sync_status(stream=None):
     """Synchronise the stream and raise if a kernel reported a device timeout."""
     _check(fa_sync_status(_stream_handle(stream)), "device status")
+
+
+# ---------------------------------------------------------------------------
+# FP8 forward
+# ---------------------------------------------------------------------------
+
+def fp8_workspace_bytes(B, H, N, d=128) -> int:
+    return int(fa_fp8_workspace_size(B, H, N, d))
+
+
+def _r256(x: int) -> int:
+    return (x + 255) & ~255
+
+
+def fp8_workspace_views(ws, B, H, N):
+    """Typed views of an FP8 workspace (uint8 CUDA tensor) in the layout fa.h
+    documents: q8, k8 [BH, npad, 128] and vt8 [BH, 128, npad] (uint8 E4M3 codes),
+    sq, sk, sv, vfold [BH, T], vmax [BH] and amax [3] (fp32)."""
+    torch = _torch()
+    BH, T = B * H, (N + 127) // 128
+    npad = 128 * T
+    codes = _r256(BH * npad * 128)
+    per_tile = _r256(BH * T * 4)
+    off = 0
+    out = {}
+    for name in ("q8", "k8", "vt8"):
+        out[name] = ws[off:off + BH * npad * 128]
+        off += codes
+    out["q8"] = out["q8"].view(BH, npad, 128)
+    out["k8"] = out["k8"].view(BH, npad, 128)
+    out["vt8"] = out["vt8"].view(BH, 128, npad)
+    for name in ("sq", "sk", "sv", "vfold"):
+        out[name] = ws[off:off + BH * T * 4].view(torch.float32).view(BH, T)
+        off += per_tile
+    out["vmax"] = ws[off:off + BH * 4].view(torch.float32)
+    off += _r256(BH * 4)
+    out["amax"] = ws[off:off + 12].view(torch.float32)
+    return out
+
+
+def sign_words(bits):
+    """Four uint32 words (bit j set: s_j = -1) as the ctypes array fa_fp8_quantize takes."""
+    words = [int(x) & 0xFFFFFFFF for x in bits]
+    if len(words) != 4:
+        raise ValueError("signs are four 32-bit words (head dimension 128)")
+    return (ctypes.c_uint32 * 4)(*words)
+
+
+def quantize_fp8(q, k, v, signs=None, rotate=True, per_tensor=False, workspace=None, stream=None):
+    """Fill an FP8 workspace from bf16 q, k, v [B, H, N, 128].  signs: four
+    uint32 words of random sign bits (required when rotate).  Returns the
+    workspace (uint8 CUDA tensor)."""
+    torch = _torch()
+    B, H, N, d = _check_qkv(q, k, v)
+    nbytes = fp8_workspace_bytes(B, H, N, d)
+    if nbytes == 0:
+        raise ValueError("the FP8 forward supports head dimension 128 only")
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    flags = (FA_FP8_ROTATE if rotate else 0) | (FA_FP8_PER_TENSOR if per_tensor else 0)
+    if rotate and signs is None:
+        raise ValueError("rotate=True needs the random sign words")
+    sw = sign_words(signs) if rotate else None
+    rc = fa_fp8_quantize(q.data_ptr(), k.data_ptr(), v.data_ptr(), B, H, N, d, sw, flags,
+                         workspace.data_ptr(), workspace.numel(), _stream_handle(stream))
+    _check(rc, "fa_fp8_quantize")
+    return workspace
+
+
+def forward_fp8_quantized(workspace, B, H, N, scale=None, causal=False, out=None, lse=None,
+                          device=None, stream=None):
+    """Attention from a filled FP8 workspace.  Returns (o bf16, lse fp32)."""
+    torch = _torch()
+    d = 128
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    device = workspace.device if device is None else device
+    if out is None:
+        out = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=device)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=device)
+    if out.dtype != torch.bfloat16 or not out.is_contiguous() or tuple(out.shape) != (B, H, N, d):
+        raise ValueError("out must be contiguous bf16 [B, H, N, 128]")
+    if lse.dtype != torch.float32 or not lse.is_contiguous() or tuple(lse.shape) != (B, H, N):
+        raise ValueError("lse must be contiguous fp32 [B, H, N]")
+    rc = fa_fwd_fp8(workspace.data_ptr(), workspace.numel(), out.data_ptr(), lse.data_ptr(),
+                    B, H, N, d, scale, int(bool(causal)), _stream_handle(stream))
+    _check(rc, "fa_fwd_fp8")
+    return out, lse
+
+
+def forward_fp8(q, k, v, signs=None, scale=None, causal=False, rotate=True, per_tensor=False,
+                workspace=None, out=None, lse=None, stream=None):
+    """FP8 attention: quantize (optionally rotating Q and K), then the FP8
+    forward.  Returns (o bf16 [B,H,N,128], lse fp32 [B,H,N])."""
+    B, H, N, d = _check_qkv(q, k, v)
+    ws = quantize_fp8(q, k, v, signs=signs, rotate=rotate, per_tensor=per_tensor,
+                      workspace=workspace, stream=stream)
+    return forward_fp8_quantized(ws, B, H, N, scale=scale, causal=causal, out=out, lse=lse,
+                                 device=q.device, stream=stream)
 
 
 # ---------------------------------------------------------------------------

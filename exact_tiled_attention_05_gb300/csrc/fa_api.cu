@@ -109,6 +109,23 @@ int make_map(CUtensorMap* map, const void* ptr, int BH, int N, int d) {
     return r == CUDA_SUCCESS ? kOk : kErrCuda;
 }
 
+// uint8 tensor [z, y, x] -> 3-D map (x, y, z), box 128 x 128 x 1, 128 B swizzle
+// (one FP8 tile of 128 rows by 128 bytes).
+int make_map_u8(CUtensorMap* map, const void* ptr, int x, int y, int z) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return kErrCuda;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(x), static_cast<cuuint64_t>(y),
+                          static_cast<cuuint64_t>(z)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(x),
+                             static_cast<cuuint64_t>(x) * static_cast<cuuint64_t>(y)};
+    cuuint32_t box[3] = {128, 128, 1};
+    cuuint32_t elem[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides,
+                     box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? kOk : kErrCuda;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int check_shape(int B, int H, int N, int d, float scale, int causal) {
@@ -129,6 +146,58 @@ size_t ws_half(int B, int H, int N) {
     return round256(static_cast<size_t>(B) * H * ((N + 127) / 128) * 128 * sizeof(float));
 }
 size_t ws_bytes(int B, int H, int N) { return 2 * ws_half(B, H, N); }
+
+// FP8 workspace: segment offsets (each 256-byte aligned), in the order fa.h lists.
+struct Fp8Layout {
+    size_t q8, k8, vt8, sq, sk, sv, vfold, vmax, amax, total;
+};
+Fp8Layout fp8_layout(int B, int H, int N) {
+    const size_t BH = static_cast<size_t>(B) * H;
+    const size_t T = (static_cast<size_t>(N) + 127) / 128;
+    const size_t codes = round256(BH * T * 128 * 128);
+    const size_t per_tile = round256(BH * T * sizeof(float));
+    Fp8Layout l{};
+    size_t o = 0;
+    l.q8 = o; o += codes;
+    l.k8 = o; o += codes;
+    l.vt8 = o; o += codes;
+    l.sq = o; o += per_tile;
+    l.sk = o; o += per_tile;
+    l.sv = o; o += per_tile;
+    l.vfold = o; o += per_tile;
+    l.vmax = o; o += round256(BH * sizeof(float));
+    l.amax = o; o += 256;
+    l.total = o;
+    return l;
+}
+
+int fp8_shape(int B, int H, int N, int d) {
+    if (B < 1 || H < 1 || N < 1) return kErrInvalidArg;
+    if (d != 128) return kErrUnsupported;
+    const int64_t rows = static_cast<int64_t>(B) * H * ((static_cast<int64_t>(N) + 127) / 128) * 128;
+    if (rows * 128 >= (int64_t(1) << 31)) return kErrInvalidArg;
+    return kOk;
+}
+
+// Points the workspace members of Fp8Args into the workspace.
+int fp8_workspace(Fp8Args& a, int B, int H, int N, const void* ws, size_t bytes) {
+    const Fp8Layout l = fp8_layout(B, H, N);
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0 || bytes < l.total) return kErrWorkspace;
+    uint8_t* base = static_cast<uint8_t*>(const_cast<void*>(ws));
+    a.q8 = base + l.q8;
+    a.k8 = base + l.k8;
+    a.vt8 = base + l.vt8;
+    a.sq = reinterpret_cast<float*>(base + l.sq);
+    a.sk = reinterpret_cast<float*>(base + l.sk);
+    a.sv = reinterpret_cast<float*>(base + l.sv);
+    a.vfold = reinterpret_cast<float*>(base + l.vfold);
+    a.vmax = reinterpret_cast<float*>(base + l.vmax);
+    a.amax = reinterpret_cast<float*>(base + l.amax);
+    a.BH = B * H;
+    a.N = N;
+    a.n_tiles = (N + 127) / 128;
+    return kOk;
+}
 
 int map_cuda(cudaError_t e) { return e == cudaSuccess ? kOk : kErrCuda; }
 
@@ -187,7 +256,7 @@ using namespace fa;
 
 extern "C" {
 
-int fa_version(void) { return 200; }
+int fa_version(void) { return 300; }
 
 const char* fa_status_string(int status) {
     switch (status) {
@@ -295,6 +364,57 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
         return rc;
     return fa_bwd_dq(q, k, v, lse, dout, dq, B, H, N, d, scale, causal, workspace, workspace_bytes,
                      stream);
+}
+
+size_t fa_fp8_workspace_size(int B, int H, int N, int d) {
+    if (fp8_shape(B, H, N, d) != kOk) return 0;
+    return fp8_layout(B, H, N).total;
+}
+
+int fa_fp8_quantize(const void* q, const void* k, const void* v, int B, int H, int N, int d,
+                    const unsigned int* signs, int flags, void* workspace, size_t workspace_bytes,
+                    void* stream) {
+    if (!q || !k || !v) return FA_ERR_INVALID_ARG;
+    if (flags & ~(FA_FP8_ROTATE | FA_FP8_PER_TENSOR)) return FA_ERR_INVALID_ARG;
+    if ((flags & FA_FP8_ROTATE) && !signs) return FA_ERR_INVALID_ARG;
+    int rc = fp8_shape(B, H, N, d);
+    if (rc) return rc;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return FA_ERR_MISALIGNED;
+    Fp8Args a{};
+    if ((rc = fp8_workspace(a, B, H, N, workspace, workspace_bytes))) return rc;
+    if ((rc = device_ready(&a.status))) return rc;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.rotate = (flags & FA_FP8_ROTATE) ? 1 : 0;
+    a.per_tensor = (flags & FA_FP8_PER_TENSOR) ? 1 : 0;
+    for (int i = 0; i < 4; ++i) a.signs[i] = a.rotate ? signs[i] : 0u;
+    return map_cuda(launch_fp8_quant(a, static_cast<cudaStream_t>(stream)));
+}
+
+int fa_fwd_fp8(const void* workspace, size_t workspace_bytes, void* o, float* lse, int B, int H,
+               int N, int d, float scale, int causal, void* stream) {
+    if (!o || !lse) return FA_ERR_INVALID_ARG;
+    int rc = fp8_shape(B, H, N, d);
+    if (rc) return rc;
+    if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+    if (!aligned16(o) || (reinterpret_cast<uintptr_t>(lse) & 3u)) return FA_ERR_MISALIGNED;
+    Fp8Args a{};
+    if ((rc = fp8_workspace(a, B, H, N, workspace, workspace_bytes))) return rc;
+    if ((rc = device_ready(&a.status))) return rc;
+    const int BH = B * H;
+    const int npad = a.n_tiles * 128;
+    CUtensorMap tq, tk, tvt, to;
+    if ((rc = make_map_u8(&tq, a.q8, 128, npad, BH)) || (rc = make_map_u8(&tk, a.k8, 128, npad, BH)) ||
+        (rc = make_map_u8(&tvt, a.vt8, npad, 128, BH)) || (rc = make_map(&to, o, BH, N, 128)))
+        return rc;
+    a.lse = lse;
+    a.n_qblk = (N + 255) / 256;
+    a.group = clampi(floor_pow2(clampi((2 * current_sms()) / a.n_qblk, 1, 1 << 20)), 1, BH);
+    a.causal = causal;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    return map_cuda(launch_fwd_fp8(tq, tk, tvt, to, a, static_cast<cudaStream_t>(stream)));
 }
 
 int fa_sync_status(void* stream) {

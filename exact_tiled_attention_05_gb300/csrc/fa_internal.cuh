@@ -71,6 +71,36 @@ struct BwdArgs {
     int* status;
 };
 
+// FP8 forward (d = 128).  The quantizer reads q, k, v and fills the FP8
+// workspace; the attention kernel reads the workspace and writes o and lse.
+// Rows are padded to npad = n_tiles * 128 (padding rows hold code 0).
+struct Fp8Args {
+    const void* q;    // bf16 [BH, N, 128]
+    const void* k;
+    const void* v;
+    uint8_t* q8;      // E4M3 [BH, npad, 128], rows rotated when `rotate`
+    uint8_t* k8;      // E4M3 [BH, npad, 128]
+    uint8_t* vt8;     // E4M3 [BH, 128, npad]: V^T, keys permuted within each tile
+    float* sq;        // fp32 [BH, n_tiles]: per-tile scales (value = code * scale)
+    float* sk;
+    float* sv;
+    float* vfold;     // fp32 [BH, n_tiles]: sv / vmax
+    float* vmax;      // fp32 [BH]
+    float* amax;      // fp32 [3]: per-tensor |x| maxima (per-tensor mode only)
+    float* lse;       // fp32 [BH, N]
+    uint32_t signs[4];  // bit j set: column j of Q and K is negated before the Hadamard transform
+    int BH;
+    int N;
+    int n_tiles;      // ceil(N / 128)
+    int n_qblk;       // query blocks (256 rows each) per head
+    int group;        // causal launch order: heads per group
+    int causal;
+    int rotate;       // 1: random-sign Hadamard rotation of Q and K rows
+    int per_tensor;   // 1: one scale per tensor instead of one per tile
+    float scale_log2; // scale * log2(e)
+    int* status;
+};
+
 // Tensor maps for one [BH, N, d] bf16 tensor: box of 64 columns x 128 rows,
 // 128-byte swizzle (what the UMMA shared-memory descriptors expect).
 struct TensorMaps3 {
@@ -80,6 +110,9 @@ struct TensorMaps3 {
 // Launchers (defined in the kernel translation units).  Return a cudaError_t.
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& to, const FwdArgs& args, cudaStream_t stream);
+cudaError_t launch_fp8_quant(const Fp8Args& args, cudaStream_t stream);
+cudaError_t launch_fwd_fp8(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tvt,
+                           const CUtensorMap& to, const Fp8Args& args, cudaStream_t stream);
 cudaError_t launch_bwd_prep(int d, const BwdArgs& args, cudaStream_t stream);
 cudaError_t launch_bwd_dkdv(int d, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdk,

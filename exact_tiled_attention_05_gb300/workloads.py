@@ -135,6 +135,45 @@ def worked_example_inputs(d: int = 64, device="cpu"):
     return {"q": q.to(device), "k": k.to(device), "v": v.to(device)}
 
 
+def sign_bits(seed: int, d: int = 128) -> np.ndarray:
+    """Random signs for the FP8 path's Hadamard rotation, as d/32 uint32 words
+    (bit j set: s_j = -1): d fair coin flips from a CPU generator seeded
+    ``seed``."""
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    flips = torch.randint(0, 2, (d,), generator=g).numpy().astype(np.uint64)
+    words = np.zeros(d // 32, dtype=np.uint64)
+    for j in range(d):
+        words[j // 32] |= flips[j] << np.uint64(j % 32)
+    return words.astype(np.uint32)
+
+
+def outlier_inputs(B: int, H: int, N: int, d: int, seed: int, kind: str = "entries",
+                   device="cpu"):
+    """Q, K, V with simulated outlier features (bf16 [B,H,N,d]).
+
+    kind "entries": every entry is N(0, 1) plus, with probability 0.001, an
+    extra N(0, 10^2) term (independently in Q, K and V).
+    kind "channels": N(0, 1) entries, except that 4 feature channels (drawn
+    once per seed, the same for Q and K and for every head and row) have
+    standard deviation 5 in Q and K; V is plain N(0, 1)."""
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    shape = (B, H, N, d)
+    q = torch.randn(shape, generator=g, dtype=torch.float32)
+    k = torch.randn(shape, generator=g, dtype=torch.float32)
+    v = torch.randn(shape, generator=g, dtype=torch.float32)
+    if kind == "entries":
+        for t in (q, k, v):
+            hit = torch.rand(shape, generator=g) < 0.001
+            t += hit * torch.randn(shape, generator=g, dtype=torch.float32) * 10.0
+    elif kind == "channels":
+        ch = torch.randperm(d, generator=g)[:4]
+        q[..., ch] *= 5.0
+        k[..., ch] *= 5.0
+    else:
+        raise ValueError(f"unknown outlier kind {kind!r}")
+    return {n: t.to(torch.bfloat16).to(device) for n, t in (("q", q), ("k", k), ("v", v))}
+
+
 def bf16_bits(t: torch.Tensor) -> np.ndarray:
     """The raw bf16 bit patterns of a tensor as a uint16 numpy array [BH, N, d]."""
     t = t.detach().to("cpu").contiguous()

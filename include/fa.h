@@ -114,6 +114,57 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
                    const void* dout, void* dq, void* dk, void* dv,
                    int B, int H, int N, int d, float scale, int causal, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * FP8 forward ("FlashAttention 1–4" §"FlashAttention-3", paragraph "FP8 with
+ * block quantization and incoherent processing").  Head dimension 128 only.
+ *
+ * Two calls: fa_fp8_quantize turns bf16 q, k, v into E4M3 codes with one fp32
+ * scale per 128-row tile (value = code * scale, scale = amax / 448 over the
+ * tile), optionally after rotating every row of Q and K by the same orthogonal
+ * M = diag(s) H / sqrt(128) (s = random signs, H = Sylvester Hadamard matrix),
+ * which leaves Q K^T unchanged; fa_fwd_fp8 then runs attention on the codes
+ * with FP8 tensor-core products and writes o (bf16) and lse (fp32) with the
+ * meanings of fa_fwd.  Inside, the probabilities P are also rounded to E4M3
+ * (after multiplying by 16 and by V's per-tile scale over its largest per-tile
+ * scale) for the P V product; the row sums and lse use fp32 P.
+ *
+ * Workspace (caller-owned device memory, 256-byte aligned, at least
+ * fa_fp8_workspace_size bytes).  With BH = B*H, T = ceil(N / 128) and
+ * npad = 128 T, it holds these segments in order, each starting on a 256-byte
+ * boundary:
+ *   q8   uint8 [BH, npad, 128]  E4M3 codes of (rotated) Q; rows >= N are 0
+ *   k8   uint8 [BH, npad, 128]  E4M3 codes of (rotated) K
+ *   vt8  uint8 [BH, 128, npad]  E4M3 codes of V transposed: byte (b, c, 128 t + i)
+ *                               is V row 128 t + key(i), column c, where for
+ *                               i = 4 (16 h + 4 w + x) + e (h < 2, w < 4, x < 4, e < 4)
+ *                               key(i) = 64 h + 32 (e / 2) + 8 w + 2 x + e % 2
+ *   sq, sk, sv  fp32 [BH, T]    per-tile scales of Q, K, V
+ *   vfold fp32 [BH, T]          sv / vmax
+ *   vmax  fp32 [BH]             largest sv of the head
+ *   amax  fp32 [4]              per-tensor |x| maxima of Q, K, V (FA_FP8_PER_TENSOR)
+ * --------------------------------------------------------------------------- */
+#define FA_FP8_ROTATE 1     /* rotate Q and K rows by diag(s) H / sqrt(128) */
+#define FA_FP8_PER_TENSOR 2 /* one scale per tensor (the pages' baseline) instead of per tile */
+
+/* Bytes of FP8 workspace for these sizes (0 for d != 128 or non-positive sizes). */
+size_t fa_fp8_workspace_size(int B, int H, int N, int d);
+
+/* Quantize q, k, v (bf16 [B,H,N,128]) into the workspace.  signs: host array
+ * of 4 uint32 words, bit j (word j/32, bit j%32) set means s_j = -1; read
+ * during the call, may be NULL when FA_FP8_ROTATE is not in flags.  flags: an
+ * OR of FA_FP8_ROTATE and FA_FP8_PER_TENSOR.  Errors: FA_ERR_UNSUPPORTED for
+ * d != 128, FA_ERR_WORKSPACE for a missing, misaligned or small workspace,
+ * FA_ERR_INVALID_ARG for unknown flags or a NULL signs with FA_FP8_ROTATE. */
+int fa_fp8_quantize(const void* q, const void* k, const void* v, int B, int H, int N, int d,
+                    const unsigned int* signs, int flags, void* workspace,
+                    size_t workspace_bytes, void* stream);
+
+/* Attention on a workspace that fa_fp8_quantize filled for the same B, H, N, d
+ * (on the same stream, or ordered before this call).  Writes o (bf16
+ * [B,H,N,128]) and lse (fp32 [B,H,N]); scale and causal as for fa_fwd. */
+int fa_fwd_fp8(const void* workspace, size_t workspace_bytes, void* o, float* lse,
+               int B, int H, int N, int d, float scale, int causal, void* stream);
+
 /* Synchronises `stream`, then returns and clears the device status word of the
  * current device: FA_OK, or FA_ERR_DEVICE_TIMEOUT if any kernel gave up on a
  * wait since the last call, or FA_ERR_CUDA if the synchronisation failed. */

@@ -446,6 +446,10 @@ def run_gpu(args, world, rank, local):
                 "pct_of_bf16_peak": 100.0 * f_gate / peak_burst,
                 "gate": ">= 60% of dense BF16 peak"}
 
+    # ---------------- FP8 forward (quantize + FP8 attention), same workload ----------------
+    fp8 = fp8_forward_timing(fa, wl, wg, gin, dev, stream, peak_burst)
+    check(fa.fa_sync_status(h), "fp8 forward")
+
     del gin, go, gl
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
@@ -456,7 +460,7 @@ def run_gpu(args, world, rank, local):
         "peak_bf16_tflops": peak_burst, "peak_source": peak_src,
         "kernel_ms": per, "roofline": roofline, "e2e": e2e,
         "gpu_launches": 4 * args.steps,
-        "clocks": clk, "forward_gate": fwd_gate,
+        "clocks": clk, "forward_gate": fwd_gate, "fp8_forward": fp8,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = oracle_baseline(w, cpu_in)
@@ -464,18 +468,68 @@ def run_gpu(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
+def fp8_forward_timing(fa, wl, wg, gin, dev, stream, peak_bf16, reps=50):
+    """FP8 forward on the forward-gate workload: per-tile E4M3 quantization with
+    the random-sign Hadamard rotation (fa_fp8_quantize), then the FP8 attention
+    (fa_fwd_fp8).  Medians of CUDA-event times over `reps` launches each; the
+    FP8 dense peak is the measured bf16 peak times the nominal FP8/BF16 ratio 2."""
+    import torch
+    B, H, N = wg.B, wg.H, wg.N
+    words = wl.sign_bits(wg.seed + 7)
+    ws = torch.empty(fa.fp8_workspace_bytes(B, H, N), dtype=torch.uint8, device=dev)
+    o = torch.empty_like(gin["q"])
+    lse = torch.empty(B, H, N, dtype=torch.float32, device=dev)
+    quant = lambda: fa.quantize_fp8(gin["q"], gin["k"], gin["v"], signs=words, workspace=ws)
+    attn = lambda: fa.forward_fp8_quantized(ws, B, H, N, causal=True, out=o, lse=lse)
+    for _ in range(3):
+        quant()
+        attn()
+
+    def median_ms(fn):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(reps)]
+        torch.cuda.synchronize(dev)
+        for a_, b_ in ev:
+            a_.record(stream)
+            fn()
+            b_.record(stream)
+        torch.cuda.synchronize(dev)
+        return sorted(a_.elapsed_time(b_) for a_, b_ in ev)[reps // 2]
+
+    t_attn, t_quant = median_ms(attn), median_ms(quant)
+    flops = fwd_flops(wg)
+    tf = flops / (t_attn / 1e3) / 1e12
+    peak_fp8 = 2.0 * peak_bf16
+    return {"workload": f"fwd B={B} H={H} N={N} d={wg.d} K x3 causal, Q/K rotated, per-tile E4M3 scales",
+            "attention_ms_median": t_attn, "quantize_ms_median": t_quant,
+            "tflops": tf, "tflops_incl_quantize": flops / ((t_attn + t_quant) / 1e3) / 1e12,
+            "pct_of_fp8_peak": 100.0 * tf / peak_fp8,
+            "peak_fp8_tflops": peak_fp8, "peak_fp8_source": "measured bf16 peak x 2 (nominal FP8/BF16 ratio)"}
+
+
 def run_only(args, local):
     """Untimed launches of one part of the path, for profilers: `fwd` runs the
     forward on the N=8192 d=128 K x3 causal workload, `fwd64` the non-causal
     forward on B=4 H=16 N=2048 d=64, `bwd` the backward (prep, main, dq)
-    on the fwd+bwd workload.  W + K launches each."""
+    on the fwd+bwd workload, `fp8` the FP8 quantization (Q/K, V, fold kernels)
+    and FP8 attention on the first workload.  W + K launches each."""
     import torch
     import exact_tiled_attention_05_gb300 as fa
     from exact_tiled_attention_05_gb300 import workloads as wl
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     fa.load_library()
-    if args.only in ("fwd", "fwd64"):
+    if args.only == "fp8":
+        w = wl.WORKLOADS[FWD_GATE_WORKLOAD]
+        inp = wl.make_inputs(w, device=dev)
+        words = wl.sign_bits(w.seed + 7)
+        ws = torch.empty(fa.fp8_workspace_bytes(w.B, w.H, w.N), dtype=torch.uint8, device=dev)
+        o = torch.empty_like(inp["q"])
+        lse = torch.empty(w.B, w.H, w.N, dtype=torch.float32, device=dev)
+        for _ in range(args.warmup + args.steps):
+            fa.quantize_fp8(inp["q"], inp["k"], inp["v"], signs=words, workspace=ws)
+            fa.forward_fp8_quantized(ws, w.B, w.H, w.N, causal=True, out=o, lse=lse)
+    elif args.only in ("fwd", "fwd64"):
         w = wl.WORKLOADS[FWD_GATE_WORKLOAD if args.only == "fwd" else "fwd_2k_d64"]
         causal = args.only == "fwd"
         inp = wl.make_inputs(w, device=dev)
@@ -505,7 +559,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-budget-s", type=float, default=120.0,
                     help="--impl reference: seconds of oracle work for the whole run")
-    ap.add_argument("--only", choices=("fwd", "fwd64", "bwd"), default=None,
+    ap.add_argument("--only", choices=("fwd", "fwd64", "bwd", "fp8"), default=None,
                     help="untimed launches of one part of the path (for profilers)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl != "reference" and not args.only:

@@ -7,11 +7,11 @@
 // (random signs, then a Hadamard transform) before quantizing, which leaves
 // Q K^T unchanged while spreading outlier channels over all coordinates.
 //
-// Stage 1, fa_fp8_quant_kernel (one CTA per (tensor, head, 128-row tile)):
-//   Q, K: rows rotated in fp32 (sign flips, seven butterfly stages, * 1/sqrt(d)),
-//   V: not rotated; scale = amax / 448 over the tile (or over the whole tensor
-//   for the per-tensor baseline the page compares against), codes =
-//   e4m3(x / scale).  Q and K codes keep the
+// Stage 1, fa_fp8_quant_qk_kernel / fa_fp8_quant_v_kernel (one CTA per
+//   (tensor, head, 128-row tile)): Q, K rows rotated in fp32 (sign flips, seven
+//   butterfly stages, * 1/sqrt(d)), V not rotated; scale = amax / 448 over the
+//   tile (or over the whole tensor for the per-tensor baseline the page
+//   compares against), codes = e4m3(x * (448 / amax)).  Q and K codes keep the
 //   [BH, N, d] layout; V is written transposed, [BH, d, N], with the keys of
 //   each 128-key tile in the order the forward kernel packs P (below).
 // Stage 2, fa_fp8_vfold_kernel: per head, vmax = max over tiles of V's scale
@@ -19,22 +19,26 @@
 // Stage 3, fa_fwd_fp8_kernel: the bf16 forward's structure (two 128-row Q tiles
 //   per CTA, four softmax threads per row in one warp, P handed over in two
 //   parts, conditional rescaling) with tcgen05.mma kind::f8f6f4: S = Q8 K8^T
-//   (four k-steps of 32), s = S * scale_q * scale_k, P = exp2(.) in fp32 for the
-//   row sums, P * fold_j * 16 quantized to E4M3 in TMEM, O += P8 V8^T; at the
-//   end O * vmax / (16 l).  lse as the bf16 forward.
+//   (four k-steps of 32), s = S * scale_q * scale_k, P * c_j = exp2(s - m +
+//   log2 c_j) in fp32 (c_j = 16 fold_j) quantized to E4M3 into shared memory,
+//   O += P8 V8^T, row sums l = sum_j (sum P * c_j) / c_j; at the end
+//   O * vmax / (16 l).  lse as the bf16 forward.
 //
 // P's range.  The running max is raised only when a tile's max exceeds it by
 // more than tau = 4 (log2 units), so P <= 2^tau; the factor 2^(8 - tau) = 16
 // puts the largest P * fold at or below 256 (E4M3 saturates at 448) while
 // keeping weights down to 2^-10 of the row max in E4M3's normal range.
 //
-// P packing.  A TMEM column of an 8-bit A operand holds four consecutive
-// K-indices.  A softmax thread holds keys 8i + 2c + {0, 1} (c = lane % 4) of
-// its two rows, so it packs keys {8w + 2c, +1} of repetition w and
-// {8(w+4) + 2c, +1} of repetition w + 4 into one word, stored at column
-// 16h + 4w + c of part h (keys 64h..64h+63).  The K-index order of P is thus a
-// fixed permutation of the tile's keys; V^T is written in the same order, and
-// sum_k P[., k] V[k, .] does not depend on the order.
+// Pipeline.  P goes to shared memory (two buffers per Q tile), not over S in
+// TMEM, so S(j+1) may overwrite S(j) as soon as the softmax threads hold S(j)
+// in registers: the tensor core computes S(j+1) while the softmax of step j
+// runs, and P(j) V_j is an SS product.
+//
+// P layout.  A softmax thread holds keys 8i + 2c + {0, 1} (i < 16, c = lane % 4)
+// of its two rows.  For part h (i = 8h .. 8h + 7) it writes, per row, one
+// 16-byte chunk: K position 64h + 16c + 2(i - 8h) + e holds key 8i + 2c + e.
+// The K order of P is thus a fixed permutation of the tile's keys; V^T is
+// written in the same order, and sum_k P[., k] V[k, .] does not depend on it.
 #include "fa_internal.cuh"
 #include "ptx.cuh"
 
@@ -94,31 +98,17 @@ __device__ __forceinline__ void umma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uin
         : "memory");
 }
 
-// D[tmem] (+)= A[tmem] * B[smem]^T, both E4M3.
-__device__ __forceinline__ void umma_ts_f8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                           uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n"
-        " .reg .pred p;\n"
-        " setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n"
-        "}\n" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
 // Instruction descriptor of kind::f8f6f4 with E4M3 A and B (format code 0 at
 // bits 7 and 10), fp32 D, both operands K-major.
 __host__ __device__ constexpr uint32_t idesc_e4m3_f32(uint32_t M, uint32_t N) {
     return (1u << 4) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
-// Key order of P's K-indices within a 128-key tile (see the file comment):
-// K-index 4c + e, c = 16h + 4w + q, holds key 64h + 32(e >> 1) + 8w + 2q + (e & 1).
-__host__ __device__ __forceinline__ int p_key_of_index(int kidx) {
-    const int c = kidx >> 2, e = kidx & 3;
-    const int h = c >> 4, w = (c >> 2) & 3, q = c & 3;
-    return 64 * h + 32 * (e >> 1) + 8 * w + 2 * q + (e & 1);
+// Key order of P's K positions within a 128-key tile (see the file comment):
+// position 64h + 16c + 2i + e holds key 64h + 8i + 2c + e.
+__host__ __device__ __forceinline__ int p_key_of_index(int kpos) {
+    const int h = kpos >> 6, c = (kpos >> 4) & 3, i = (kpos >> 1) & 7, e = kpos & 1;
+    return 64 * h + 8 * i + 2 * c + e;
 }
 
 __device__ __forceinline__ void st_shared_b32(uint32_t addr, uint32_t v) {
@@ -158,119 +148,169 @@ __device__ __forceinline__ void tmem_st_16x256b_x4(uint32_t taddr, const uint32_
         : "memory");
 }
 
-// 16x128b, four repetitions: registers 2r, 2r + 1 go to column 4r + lane % 4 of
-// rows lane/4 and lane/4 + 8.
-__device__ __forceinline__ void tmem_st_16x128b_x4(uint32_t taddr, const uint32_t (&r)[8]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.16x128b.x4.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
-        : "memory");
-}
-
 // ---------------------------------------------------------------------------
 // Stage 1: rotation and block quantization
 // ---------------------------------------------------------------------------
-// grid (tiles, BH, 3 tensors), 256 threads; warp w takes rows w, w + 8, ..;
-// lane l holds columns 4l..4l+3 of a row.  MODE 0 only reduces |x| of the tile
-// into amax[tensor] (per-tensor baseline, first pass); MODE 1 quantizes.
+// Both kernels: 256 threads, 8 threads per row, thread g = lane % 8 of a row
+// holds its 16 columns 16g .. 16g + 15; a warp covers 4 rows and the CTA 32 per
+// pass, four passes cover the 128-row tile.  MODE 0 only reduces |x| of the
+// tile into amax[tensor] (per-tensor baseline, first pass); MODE 1 quantizes:
+// scale = amax / 448 and code = e4m3(x * (448 / amax)) (scale 1 and factor 1
+// for an all-zero tile).
+
+// |x| maximum of the CTA (all threads call; returns the same value to all).
+__device__ __forceinline__ float cta_amax(float m, float* red) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    float r = red[0];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) r = fmaxf(r, red[w]);
+    return r;
+}
+
+// Loads 16 bf16 columns of four rows (one per pass) as fp32; rows past N are 0.
+__device__ __forceinline__ void load_rows16(const uint16_t* src, int N, int row0, int g, float (&x)[4][16]) {
+    uint4 raw[4][2];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        const int row = row0 + 32 * p;
+        const uint4* ptr = reinterpret_cast<const uint4*>(src + static_cast<size_t>(row) * kHD + 16 * g);
+        raw[p][0] = row < N ? __ldg(ptr) : make_uint4(0u, 0u, 0u, 0u);
+        raw[p][1] = row < N ? __ldg(ptr + 1) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        const uint32_t w[8] = {raw[p][0].x, raw[p][0].y, raw[p][0].z, raw[p][0].w,
+                               raw[p][1].x, raw[p][1].y, raw[p][1].z, raw[p][1].w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            x[p][2 * i] = __uint_as_float(w[i] << 16);
+            x[p][2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    }
+}
+
+// grid (tiles, BH, 2): Q (z = 0) and K (z = 1).
 template <int MODE>
-__global__ void __launch_bounds__(256) fa_fp8_quant_kernel(const __grid_constant__ Fp8Args a) {
-    extern __shared__ float tl[];  // [128][129] fp32 tile (row stride 129 against bank conflicts)
+__global__ void __launch_bounds__(256) fa_fp8_quant_qk_kernel(const __grid_constant__ Fp8Args a) {
     __shared__ float red[8];
     const int tile = static_cast<int>(blockIdx.x);
     const int bh = static_cast<int>(blockIdx.y);
-    const int which = static_cast<int>(blockIdx.z);  // 0 Q, 1 K, 2 V
+    const int which = static_cast<int>(blockIdx.z);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane & 7;
     const int N = a.N, npad = a.n_tiles * 128;
-    const bool rot = a.rotate != 0 && which < 2;
-    const uint16_t* src = static_cast<const uint16_t*>(which == 0 ? a.q : which == 1 ? a.k : a.v) +
-                          static_cast<size_t>(bh) * N * kHD;
-    float sgn[4];
+    const int row0 = tile * 128 + warp * 4 + (lane >> 3);  // + 32 p
+    const uint16_t* src = static_cast<const uint16_t*>(which == 0 ? a.q : a.k) + static_cast<size_t>(bh) * N * kHD;
+    float x[4][16];
+    load_rows16(src, N, row0, g, x);
+    if (a.rotate) {
+        // column 16g + e is negated when bit 16(g % 2) + e of word g / 2 is set
+        const uint32_t sbits = a.signs[g >> 1] >> (16 * (g & 1));
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        const int col = 4 * lane + e;
-        sgn[e] = ((a.signs[col >> 5] >> (col & 31)) & 1u) ? -1.f : 1.f;
-    }
-    float amax = 0.f;
-    for (int r = warp; r < 128; r += 8) {
-        const int row = tile * 128 + r;
-        float x[4] = {0.f, 0.f, 0.f, 0.f};
-        if (row < N) {
-            const uint2 w = __ldg(reinterpret_cast<const uint2*>(src + static_cast<size_t>(row) * kHD) + lane);
-            x[0] = __uint_as_float(w.x << 16);
-            x[1] = __uint_as_float(w.x & 0xffff0000u);
-            x[2] = __uint_as_float(w.y << 16);
-            x[3] = __uint_as_float(w.y & 0xffff0000u);
-        }
-        if (rot && row < N) {  // (rows past N stay +0; row is the same for the whole warp)
+        for (int p = 0; p < 4; ++p) {
             // sign flips, then y_i = sum_j (-1)^popcount(i & j) x_j by butterflies
-            // h = 1, 2 (inside the lane), 4 .. 64 (across lanes), then * 1/sqrt(d)
+            // h = 1, 2, 4, 8 (inside the thread) and 16, 32, 64 (across the
+            // row's 8 threads), then * 1/sqrt(d).  Every lane runs the shuffles;
+            // rows past N are zeroed afterwards.
 #pragma unroll
-            for (int e = 0; e < 4; ++e) x[e] *= sgn[e];
-            float t0 = x[0] + x[1], t1 = x[0] - x[1], t2 = x[2] + x[3], t3 = x[2] - x[3];
-            x[0] = t0 + t2;
-            x[2] = t0 - t2;
-            x[1] = t1 + t3;
-            x[3] = t1 - t3;
+            for (int e = 0; e < 16; ++e)
+                if ((sbits >> e) & 1u) x[p][e] = -x[p][e];
 #pragma unroll
-            for (int m = 1; m < 32; m <<= 1) {
+            for (int h = 1; h < 16; h <<= 1) {
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float p = __shfl_xor_sync(0xffffffffu, x[e], m);
-                    x[e] = (lane & m) ? (p - x[e]) : (x[e] + p);
+                for (int i = 0; i < 16; ++i) {
+                    if (i & h) continue;
+                    const float u = x[p][i], v = x[p][i + h];
+                    x[p][i] = u + v;
+                    x[p][i + h] = u - v;
                 }
             }
 #pragma unroll
-            for (int e = 0; e < 4; ++e) x[e] *= 0.08838834764831845f;  // 1 / sqrt(128)
-        }
+            for (int m = 1; m < 8; m <<= 1) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            tl[r * 129 + 4 * lane + e] = x[e];
-            amax = fmaxf(amax, fabsf(x[e]));
+                for (int e = 0; e < 16; ++e) {
+                    const float o = __shfl_xor_sync(0xffffffffu, x[p][e], m);
+                    x[p][e] = (g & m) ? (o - x[p][e]) : (x[p][e] + o);
+                }
+            }
+            const bool live = row0 + 32 * p < N;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) x[p][e] = live ? x[p][e] * 0.08838834764831845f : 0.f;  // 1 / sqrt(128)
         }
     }
+    float m = 0.f;
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-    if (lane == 0) red[warp] = amax;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        float m = red[0];
-        for (int w = 1; w < 8; ++w) m = fmaxf(m, red[w]);
-        red[0] = m;
-    }
-    __syncthreads();
-    const float amax_tile = red[0];
+    for (int p = 0; p < 4; ++p)
+#pragma unroll
+        for (int e = 0; e < 16; ++e) m = fmaxf(m, fabsf(x[p][e]));
+    const float amax_tile = cta_amax(m, red);
     if (MODE == 0) {
         if (threadIdx.x == 0)
             atomicMax(reinterpret_cast<unsigned int*>(a.amax + which),
                       __float_as_uint(amax_tile));  // non-negative floats order as their bits
         return;
     }
-    const float amax_used = a.per_tensor ? a.amax[which] : amax_tile;
-    const float scale = amax_used > 0.f ? amax_used / kE4M3Max : 1.f;
-    if (threadIdx.x == 0) {
-        float* scales = which == 0 ? a.sq : which == 1 ? a.sk : a.sv;
-        scales[bh * a.n_tiles + tile] = scale;
-    }
-    if (which < 2) {
-        uint8_t* dst = (which == 0 ? a.q8 : a.k8) + (static_cast<size_t>(bh) * npad + tile * 128) * kHD;
-        for (int r = warp; r < 128; r += 8) {
-            const float* x = tl + r * 129 + 4 * lane;
-            const uint32_t w = e4m3x2(x[0] / scale, x[1] / scale) | (e4m3x2(x[2] / scale, x[3] / scale) << 16);
-            reinterpret_cast<uint32_t*>(dst + static_cast<size_t>(r) * kHD)[lane] = w;
-        }
-    } else {
-        // V^T: row = head column, 128 bytes per tile in P's key order
-        uint8_t* dst = a.vt8 + static_cast<size_t>(bh) * kHD * npad + tile * 128;
-        for (int col = warp; col < kHD; col += 8) {
-            float x[4];
+    const float amax = a.per_tensor ? a.amax[which] : amax_tile;
+    const float r = amax > 0.f ? kE4M3Max / amax : 1.f;
+    if (threadIdx.x == 0)
+        (which == 0 ? a.sq : a.sk)[bh * a.n_tiles + tile] = amax > 0.f ? amax / kE4M3Max : 1.f;
+    uint8_t* dst = (which == 0 ? a.q8 : a.k8) + static_cast<size_t>(bh) * npad * kHD;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) x[e] = tl[p_key_of_index(4 * lane + e) * 129 + col];
-            const uint32_t w = e4m3x2(x[0] / scale, x[1] / scale) | (e4m3x2(x[2] / scale, x[3] / scale) << 16);
-            reinterpret_cast<uint32_t*>(dst + static_cast<size_t>(col) * npad)[lane] = w;
-        }
+    for (int p = 0; p < 4; ++p) {
+        uint32_t w[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            w[k] = e4m3x2(x[p][4 * k] * r, x[p][4 * k + 1] * r) | (e4m3x2(x[p][4 * k + 2] * r, x[p][4 * k + 3] * r) << 16);
+        *reinterpret_cast<uint4*>(dst + static_cast<size_t>(row0 + 32 * p) * kHD + 16 * g) =
+            make_uint4(w[0], w[1], w[2], w[3]);
     }
 }
+
+// grid (tiles, BH): V, written transposed ([BH, d, npad]) with each tile's keys
+// in P's order; the tile goes through shared memory for the transpose.
+template <int MODE>
+__global__ void __launch_bounds__(256) fa_fp8_quant_v_kernel(const __grid_constant__ Fp8Args a) {
+    extern __shared__ float tl[];  // [128][129] fp32 tile (row stride 129 against bank conflicts)
+    __shared__ float red[8];
+    const int tile = static_cast<int>(blockIdx.x);
+    const int bh = static_cast<int>(blockIdx.y);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane & 7;
+    const int N = a.N, npad = a.n_tiles * 128;
+    const int rl0 = warp * 4 + (lane >> 3);  // tile-local row, + 32 p
+    const uint16_t* src = static_cast<const uint16_t*>(a.v) + static_cast<size_t>(bh) * N * kHD;
+    float x[4][16];
+    load_rows16(src, N, tile * 128 + rl0, g, x);
+    float m = 0.f;
+#pragma unroll
+    for (int p = 0; p < 4; ++p)
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            m = fmaxf(m, fabsf(x[p][e]));
+            if (MODE == 1) tl[(rl0 + 32 * p) * 129 + 16 * g + e] = x[p][e];
+        }
+    const float amax_tile = cta_amax(m, red);  // (its barrier also orders the tile writes)
+    if (MODE == 0) {
+        if (threadIdx.x == 0) atomicMax(reinterpret_cast<unsigned int*>(a.amax + 2), __float_as_uint(amax_tile));
+        return;
+    }
+    const float amax = a.per_tensor ? a.amax[2] : amax_tile;
+    const float r = amax > 0.f ? kE4M3Max / amax : 1.f;
+    if (threadIdx.x == 0) a.sv[bh * a.n_tiles + tile] = amax > 0.f ? amax / kE4M3Max : 1.f;
+    // V^T: row = head column, 128 bytes per tile in P's key order
+    uint8_t* dst = a.vt8 + static_cast<size_t>(bh) * kHD * npad + tile * 128;
+    for (int col = warp; col < kHD; col += 8) {
+        float v[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) v[e] = tl[p_key_of_index(4 * lane + e) * 129 + col] * r;
+        reinterpret_cast<uint32_t*>(dst + static_cast<size_t>(col) * npad)[lane] =
+            e4m3x2(v[0], v[1]) | (e4m3x2(v[2], v[3]) << 16);
+    }
+}
+
 
 // Stage 2: per head, vmax = max_t scale_v[t] and fold[t] = scale_v[t] / vmax.
 __global__ void __launch_bounds__(32) fa_fp8_vfold_kernel(const __grid_constant__ Fp8Args a) {
@@ -287,22 +327,27 @@ __global__ void __launch_bounds__(32) fa_fp8_vfold_kernel(const __grid_constant_
 // ---------------------------------------------------------------------------
 // Stage 3: the FP8 forward
 // ---------------------------------------------------------------------------
+// Shared memory: the two Q tiles, two P buffers per Q tile (P(j) goes to
+// buffer j % 2; at the end the tile's bf16 O is staged over its two P
+// buffers, one 64-column box each) and the K_j / V_j^T ring.
 struct alignas(1024) Fp8Smem {
     uint8_t q[2][kTile8];
+    uint8_t p[2][2][kTile8];
     uint8_t kv[kStages][kTile8];
-    uint8_t o[2][2 * kOBox];  // bf16 O of each tile, two 64-column boxes
     uint64_t q_full;
     uint64_t kv_full[kStages];
     uint64_t kv_empty[kStages];
-    uint64_t s_full[2];
-    uint64_t p_full[2][2];
-    uint64_t o_done[2];
+    uint64_t s_full[2];        // S_t(j) in TMEM (MMA commit)
+    uint64_t s_free[2];        // S_t(j) read into registers (256 softmax threads)
+    uint64_t p_full[2][2][2];  // [tile][buffer][part]: P part in shared memory (256 threads)
+    uint64_t p_free[2][2];     // [tile][buffer]: the P V reading the buffer completed (MMA commit)
     uint64_t out_staged[2];
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
 };
 static_assert(sizeof(Fp8Smem) + 1024 <= 232448, "FP8 forward shared memory exceeds 227 KB");
+static_assert(2 * kTile8 == 2 * kOBox, "O is staged over a tile's two P buffers");
 
 __device__ __forceinline__ void fp8_timeout(const Fp8Args& a, volatile int* abort) {
     *abort = 1;
@@ -358,9 +403,12 @@ fa_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(smem_u32(&sm.s_full[t]), 1);
-            mbar_init(smem_u32(&sm.p_full[t][0]), kSoftmaxPerTile);
-            mbar_init(smem_u32(&sm.p_full[t][1]), kSoftmaxPerTile);
-            mbar_init(smem_u32(&sm.o_done[t]), 1);
+            mbar_init(smem_u32(&sm.s_free[t]), kSoftmaxPerTile);
+            for (int b = 0; b < 2; ++b) {
+                mbar_init(smem_u32(&sm.p_full[t][b][0]), kSoftmaxPerTile);
+                mbar_init(smem_u32(&sm.p_full[t][b][1]), kSoftmaxPerTile);
+                mbar_init(smem_u32(&sm.p_free[t][b]), 1);
+            }
             mbar_init(smem_u32(&sm.out_staged[t]), kSoftmaxPerTile);
         }
         mbar_init(smem_u32(&sm.drain), 1);
@@ -389,7 +437,7 @@ fa_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             int issued = 0;
             bool ok = true;
             const int n_loads = FA_FAULT_INJECT ? 0 : 2 * nmax;
-            for (int idx = 0; idx < n_loads; ++idx) {
+            for (int idx = 0; idx < n_loads; ++idx) {  // K_0, V_0, K_1, V_1, ..
                 const int slot = idx % kStages;
                 if (!mbar_wait(smem_u32(&sm.kv_empty[slot]), ((idx / kStages) & 1) ^ 1, kWaitTimeoutNs,
                                abort)) {
@@ -418,13 +466,15 @@ fa_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                     break;
                 }
                 for (int b = 0; b < 2; ++b)
-                    tma_store_3d(&to, smem_u32(sm.o[t]) + b * kOBox, b * 64, q0[t], bh);
+                    tma_store_3d(&to, smem_u32(sm.p[t][b]), b * 64, q0[t], bh);
             }
             bulk_commit_group();
             bulk_wait_group0();
         }
     } else if (warp == 1) {
         // ===================== MMA issuer =====================
+        // Per step j: S_t(j+1) as soon as the softmax has read S_t(j) into
+        // registers, then P_t(j) V_j from shared memory as P's parts arrive.
         if (elect_one()) {
             constexpr uint32_t idesc = idesc_e4m3_f32(kBM, kBN);  // S and O: N = 128 = d
             const uint32_t q_addr[2] = {smem_u32(sm.q[0]), smem_u32(sm.q[1])};
@@ -442,13 +492,13 @@ fa_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                                sdesc_sw128(q_addr[t] + kk * 32, 16, 1024),
                                sdesc_sw128(k_addr + kk * 32, 16, 1024), idesc, kk > 0);
             };
-            // O_t += P8_t V8: part q of P (TMEM columns 16q..16q+15 of S_t) is
-            // k-steps 2q, 2q + 1; V^T K-major (keys in P's order)
-            auto issue_pv = [&](int t, uint32_t vt_addr, int part, bool acc) {
+            // O_t += P8_t V8: part h of P (K positions 64h..64h+63) is k-steps
+            // 2h, 2h + 1; P and V^T K-major, keys in the same order
+            auto issue_pv = [&](int t, uint32_t p_addr, uint32_t vt_addr, int part, bool acc) {
 #pragma unroll
                 for (int i = 0; i < 2; ++i) {
                     const int kk = part * 2 + i;
-                    umma_ts_f8(tbase + kOCol0 + t * kHD, tbase + static_cast<uint32_t>(t) * kSColStride + kk * 8,
+                    umma_ss_f8(tbase + kOCol0 + t * kHD, sdesc_sw128(p_addr + kk * 32, 16, 1024),
                                sdesc_sw128(vt_addr + kk * 32, 16, 1024), idesc,
                                (acc || part > 0 || i > 0) ? 1u : 0u);
                 }
@@ -464,33 +514,37 @@ fa_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             }
             for (int j = 0; ok && j < nmax; ++j) {
                 const int iv = 2 * j + 1, ik = 2 * j + 2;
-                if (!(ok = wait_kv(iv))) break;
-                tc_fence_after();
-                bool k_ready = false;
-                for (int t = 0; t < 2 && ok; ++t) {
-                    if (j < nkv[t]) {
-                        for (int part = 0; part < 2 && ok; ++part) {
-                            if (!(ok = mbar_wait(smem_u32(&sm.p_full[t][part]), j & 1, kWaitTimeoutNs, abort)))
-                                break;
-                            tc_fence_after();
-                            issue_pv(t, kv_addr(iv), part, j > 0);
-                        }
-                        if (!ok) break;
-                        umma_commit(smem_u32(&sm.o_done[t]));
-                    }
-                    if (t == 1) umma_commit(smem_u32(&sm.kv_empty[iv % kStages]));
-                    if (j + 1 < nkv[t]) {
-                        if (!k_ready) {
-                            if (!(ok = wait_kv(ik))) break;
-                            tc_fence_after();
-                            k_ready = true;
-                        }
-                        // S_t(j+1) overwrites P_t(j) after PV_t(j) was issued (in order)
+                // S(j+1): overwrites S(j) once the softmax has it in registers
+                if (j + 1 < nmax) {
+                    if (!(ok = wait_kv(ik))) break;
+                    for (int t = 0; t < 2 && ok; ++t) {
+                        if (j + 1 >= nkv[t]) continue;
+                        if (!(ok = mbar_wait(smem_u32(&sm.s_free[t]), j & 1, kWaitTimeoutNs, abort))) break;
+                        tc_fence_after();
                         issue_s(t, kv_addr(ik));
                         umma_commit(smem_u32(&sm.s_full[t]));
                     }
+                    if (!ok) break;
+                    umma_commit(smem_u32(&sm.kv_empty[ik % kStages]));
                 }
-                if (ok && k_ready) umma_commit(smem_u32(&sm.kv_empty[ik % kStages]));
+                // P(j) V_j
+                if (!(ok = wait_kv(iv))) break;
+                tc_fence_after();
+                const int b = j & 1;
+                for (int t = 0; t < 2 && ok; ++t) {
+                    if (j >= nkv[t]) continue;
+                    for (int part = 0; part < 2; ++part) {
+                        if (!(ok = mbar_wait(smem_u32(&sm.p_full[t][b][part]), (j >> 1) & 1, kWaitTimeoutNs,
+                                             abort)))
+                            break;
+                        tc_fence_after();
+                        issue_pv(t, smem_u32(sm.p[t][b]), kv_addr(iv), part, j > 0);
+                    }
+                    if (!ok) break;
+                    umma_commit(smem_u32(&sm.p_free[t][b]));
+                }
+                if (!ok) break;
+                umma_commit(smem_u32(&sm.kv_empty[iv % kStages]));
             }
             if (!ok) fp8_timeout(a, abort);
             umma_commit(smem_u32(&sm.drain));
@@ -513,6 +567,10 @@ fa_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         const uint32_t lanes16 = tbase + (static_cast<uint32_t>(wq * 32 + sub * 16) << 16);
         const uint32_t s_addr = lanes16 + static_cast<uint32_t>(t) * kSColStride;
         const uint32_t o_addr = lanes16 + kOCol0 + t * kHD;
+        // P part h of rows rA / rB: the 16-byte chunk 4h + cq, 128-byte swizzle
+        const uint32_t p_row_A = static_cast<uint32_t>(rA * 128), p_row_B = static_cast<uint32_t>((rA + 8) * 128);
+        const uint32_t p_chunk[2] = {static_cast<uint32_t>(((0 + cq) ^ (rA & 7)) << 4),
+                                     static_cast<uint32_t>(((4 + cq) ^ (rA & 7)) << 4)};
         const float* skr = a.sk + static_cast<size_t>(bh) * a.n_tiles;
         const float* fold = a.vfold + static_cast<size_t>(bh) * a.n_tiles;
         // scores in log2 units: raw S (code units) * scale * log2e * scale_q * scale_k
@@ -523,9 +581,16 @@ fa_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         bool ok = true;
         for (int j = 0; j < my_nkv; ++j) {
             const float sl2 = sl2q * __ldg(skr + j);
-            const float fj = __ldg(fold + j) * kPScale;  // exact: a power of two
+            // c_j = fold_j * 16 goes into the exponent: 2^(x - m + log2 c_j) = P * c_j
+            const float cj = __ldg(fold + j) * kPScale;  // exact: a power of two
+            const float lg2c = __log2f(cj);
+            const float inv_c = __fdividef(1.0f, cj);
             const uint64_t sl2_pair = f2_pack(sl2, sl2);
-            const uint64_t f_pair = f2_pack(fj, fj);
+            const int b = j & 1;
+            if (j >= 2) {  // P buffer b was last read by P(j - 2) V (long done by now)
+                ok = mbar_wait_warp(smem_u32(&sm.p_free[t][b]), ((j >> 1) - 1) & 1, kWaitTimeoutNs, abort);
+                if (!ok) break;
+            }
             ok = mbar_wait_warp(smem_u32(&sm.s_full[t]), j & 1, kWaitTimeoutNs, abort);
             if (!ok) break;
             tc_fence_after();
@@ -535,6 +600,8 @@ fa_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             tmem_wait_ld();
             reg_fence(sa);
             reg_fence(sb);
+            tc_fence_before();
+            mbar_arrive(smem_u32(&sm.s_free[t]));  // the MMA may now write S(j+1)
 #define SR(c) ((c) < 32 ? sa[(c)] : sb[(c) - 32])
             const int kbase = j * kBN + 2 * cq;
             if ((j * kBN + kBN > N) || (a.causal && j * kBN + kBN - 1 > my_q0)) {
@@ -594,39 +661,41 @@ fa_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                     mB = mxB;
                 }
             }
-            const float negA = (mA == -INFINITY) ? 0.f : -mA;
-            const float negB = (mB == -INFINITY) ? 0.f : -mB;
+            const float negA = ((mA == -INFINITY) ? 0.f : -mA) + lg2c;
+            const float negB = ((mB == -INFINITY) ? 0.f : -mB) + lg2c;
             const uint64_t negA2 = f2_pack(negA, negA), negB2 = f2_pack(negB, negB);
+            uint64_t tA = f2_pack(0.f, 0.f), tB = f2_pack(0.f, 0.f);  // this tile's sum of P * c_j
             const bool any_rescale = __any_sync(0xffffffffu, rescale);
+            const uint32_t pbuf = smem_u32(sm.p[t][b]);
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
-                // word w of each row packs repetitions w and w + 4 of this part:
-                // keys {8w + 2cq, +1} and {8(w + 4) + 2cq, +1}
-                uint32_t pk[8];
+                // chunk of row x: repetitions 8hh .. 8hh + 7, an E4M3 pair each
+                uint32_t w[2][4];
 #pragma unroll
-                for (int w = 0; w < 4; ++w) {
+                for (int i = 0; i < 8; ++i) {
 #pragma unroll
                     for (int x = 0; x < 2; ++x) {
-                        uint32_t pair[2];
-#pragma unroll
-                        for (int r = 0; r < 2; ++r) {
-                            const int e = hh * 32 + 4 * (w + 4 * r) + 2 * x;
-                            const uint64_t x2 = f2_fma(f2_pack_u(SR(e), SR(e + 1)), sl2_pair, x == 0 ? negA2 : negB2);
-                            const float2 xv = f2_unpack(x2);
-                            const uint64_t p2 = f2_pack(ex2(xv.x), ex2(xv.y));
-                            if (x == 0)
-                                lA = f2_add(lA, p2);
-                            else
-                                lB = f2_add(lB, p2);
-                            const float2 pf = f2_unpack(f2_mul(p2, f_pair));
-                            pair[r] = e4m3x2(pf.x, pf.y);
-                        }
-                        pk[2 * w + x] = pair[0] | (pair[1] << 16);
+                        const int e = hh * 32 + 4 * i + 2 * x;
+                        const uint64_t x2 = f2_fma(f2_pack_u(SR(e), SR(e + 1)), sl2_pair, x == 0 ? negA2 : negB2);
+                        const float2 xv = f2_unpack(x2);
+                        const float p0 = ex2(xv.x), p1 = ex2(xv.y);
+                        if (x == 0)
+                            tA = f2_add(tA, f2_pack(p0, p1));
+                        else
+                            tB = f2_add(tB, f2_pack(p0, p1));
+                        const uint32_t pr = e4m3x2(p0, p1);
+                        if (i & 1)
+                            w[x][i >> 1] |= pr << 16;
+                        else
+                            w[x][i >> 1] = pr;
                     }
                 }
-                tmem_st_16x128b_x4(s_addr + hh * 16, pk);
+                st_shared_v4(pbuf + p_row_A + p_chunk[hh], w[0][0], w[0][1], w[0][2], w[0][3]);
+                st_shared_v4(pbuf + p_row_B + p_chunk[hh], w[1][0], w[1][1], w[1][2], w[1][3]);
                 if (hh == 0 && any_rescale) {
-                    ok = mbar_wait_warp(smem_u32(&sm.o_done[t]), (j - 1) & 1, kWaitTimeoutNs, abort);
+                    // O holds P V up to step j - 1: wait for that P V, then scale it
+                    // before any of step j's P V is issued (it needs P(j) part 0)
+                    ok = mbar_wait_warp(smem_u32(&sm.p_free[t][b ^ 1]), ((j - 1) >> 1) & 1, kWaitTimeoutNs, abort);
                     if (!ok) break;
                     tc_fence_after();
                     const uint64_t aA = f2_pack(alphaA, alphaA), aB = f2_pack(alphaB, alphaB);
@@ -644,18 +713,22 @@ fa_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                         }
                         tmem_st_16x256b_x4(o_addr + c * 32, r);
                     }
+                    tmem_wait_st();
+                    tc_fence_before();
                 }
-                tmem_wait_st();
-                tc_fence_before();
-                mbar_arrive(smem_u32(&sm.p_full[t][hh]));
+                fence_proxy_async_smem();
+                mbar_arrive(smem_u32(&sm.p_full[t][b][hh]));
             }
 #undef SR
             if (!ok) break;
             {
-                // the row's largest weight as P V used it: fold and scale, E4M3, back
+                const uint64_t ic2 = f2_pack(inv_c, inv_c);
+                lA = f2_fma(tA, ic2, lA);
+                lB = f2_fma(tB, ic2, lB);
+                // the row's largest weight as P V used it (E4M3) against fp32
                 const float pxA = ex2(fmaf(pmA, sl2, negA)), pxB = ex2(fmaf(pmB, sl2, negB));
-                lcA += e4m3_round(pxA * fj) / fj - pxA;
-                lcB += e4m3_round(pxB * fj) / fj - pxB;
+                lcA += (e4m3_round(pxA) - pxA) * inv_c;
+                lcB += (e4m3_round(pxB) - pxB) * inv_c;
             }
         }
         if (!ok) {
@@ -667,14 +740,16 @@ fa_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             sB += __shfl_xor_sync(0xffffffffu, sB, 1);
             sA += __shfl_xor_sync(0xffffffffu, sA, 2);
             sB += __shfl_xor_sync(0xffffffffu, sB, 2);
-            ok = mbar_wait_warp(smem_u32(&sm.o_done[t]), (my_nkv - 1) & 1, kWaitTimeoutNs, abort);
+            const int jl = my_nkv - 1;
+            ok = mbar_wait_warp(smem_u32(&sm.p_free[t][jl & 1]), (jl >> 1) & 1, kWaitTimeoutNs, abort);
             if (ok) {
                 tc_fence_after();
                 const float vmax = a.vmax[bh] * (1.0f / kPScale);
                 const float invA = vmax / (sA + lcA), invB = vmax / (sB + lcB);
-                // O rows into the tile's staging buffer: 64-column boxes of 128-byte
-                // rows, column 8i + 2cq is chunk i % 8 of box i / 8 at (i % 8) ^ (row % 8)
-                const uint32_t obuf = smem_u32(sm.o[t]);
+                // O rows into the tile's P buffers (free: every P V of the tile is
+                // done): 64-column boxes of 128-byte rows, column 8i + 2cq is chunk
+                // i % 8 of box i / 8 at (i % 8) ^ (row % 8)
+                const uint32_t obuf = smem_u32(sm.p[t][0]);
 #pragma unroll
                 for (int c = 0; c < kHD / 32; ++c) {
                     uint32_t r[16];
@@ -687,8 +762,8 @@ fa_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                         const uint32_t wb = pack_bf16x2(__uint_as_float(r[4 * i + 2]) * invB, __uint_as_float(r[4 * i + 3]) * invB);
                         const int ii = c * 4 + i;
                         const uint32_t off = static_cast<uint32_t>((ii / 8) * kOBox + (((ii % 8) ^ (rA & 7)) << 4) + 4 * cq);
-                        st_shared_b32(obuf + off + static_cast<uint32_t>(rA * 128), wa);
-                        st_shared_b32(obuf + off + static_cast<uint32_t>((rA + 8) * 128), wb);
+                        st_shared_b32(obuf + off + p_row_A, wa);
+                        st_shared_b32(obuf + off + p_row_B, wb);
                     }
                 }
                 fence_proxy_async_smem();
@@ -714,20 +789,20 @@ fa_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
 }  // namespace
 
 cudaError_t launch_fp8_quant(const Fp8Args& a, cudaStream_t stream) {
-    const size_t smem = 128 * 129 * sizeof(float);
-    cudaError_t e = cudaFuncSetAttribute(fa_fp8_quant_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(fa_fp8_quant_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(smem));
+    const size_t smem_v = 128 * 129 * sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(fa_fp8_quant_v_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem_v));
     if (e != cudaSuccess) return e;
-    const dim3 grid(static_cast<unsigned>(a.n_tiles), static_cast<unsigned>(a.BH), 3);
+    const dim3 grid_qk(static_cast<unsigned>(a.n_tiles), static_cast<unsigned>(a.BH), 2);
+    const dim3 grid_v(static_cast<unsigned>(a.n_tiles), static_cast<unsigned>(a.BH), 1);
     if (a.per_tensor) {
         if ((e = cudaMemsetAsync(a.amax, 0, 3 * sizeof(float), stream)) != cudaSuccess) return e;
-        fa_fp8_quant_kernel<0><<<grid, 256, smem, stream>>>(a);
+        fa_fp8_quant_qk_kernel<0><<<grid_qk, 256, 0, stream>>>(a);
+        fa_fp8_quant_v_kernel<0><<<grid_v, 256, 0, stream>>>(a);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    fa_fp8_quant_kernel<1><<<grid, 256, smem, stream>>>(a);
+    fa_fp8_quant_qk_kernel<1><<<grid_qk, 256, 0, stream>>>(a);
+    fa_fp8_quant_v_kernel<1><<<grid_v, 256, smem_v, stream>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     fa_fp8_vfold_kernel<<<a.BH, 32, 0, stream>>>(a);
     return cudaGetLastError();

@@ -126,7 +126,9 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
  * with FP8 tensor-core products and writes o (bf16) and lse (fp32) with the
  * meanings of fa_fwd.  Inside, the probabilities P are also rounded to E4M3
  * (after multiplying by 16 and by V's per-tile scale over its largest per-tile
- * scale) for the P V product; the row sums and lse use fp32 P.
+ * scale) for the P V product; the row sums and lse use fp32 P.  The running
+ * max is raised when a tile's max exceeds it by more than 4 (log2 units), so
+ * the largest rounded weight is 256, inside E4M3's range.
  *
  * Workspace (caller-owned device memory, 256-byte aligned, at least
  * fa_fp8_workspace_size bytes).  With BH = B*H, T = ceil(N / 128) and
@@ -136,8 +138,8 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
  *   k8   uint8 [BH, npad, 128]  E4M3 codes of (rotated) K
  *   vt8  uint8 [BH, 128, npad]  E4M3 codes of V transposed: byte (b, c, 128 t + i)
  *                               is V row 128 t + key(i), column c, where for
- *                               i = 4 (16 h + 4 w + x) + e (h < 2, w < 4, x < 4, e < 4)
- *                               key(i) = 64 h + 32 (e / 2) + 8 w + 2 x + e % 2
+ *                               i = 64 h + 16 x + 2 w + e (h, e < 2, x < 4, w < 8)
+ *                               key(i) = 64 h + 8 w + 2 x + e
  *   sq, sk, sv  fp32 [BH, T]    per-tile scales of Q, K, V
  *   vfold fp32 [BH, T]          sv / vmax
  *   vmax  fp32 [BH]             largest sv of the head

@@ -18,7 +18,9 @@ Definitions here (fp64 unless stated):
   4 exponent bits with bias 7, 3 mantissa bits, no infinities, largest finite
   448, subnormals in steps of 2^-9), values beyond 448 saturate to 448.
 * ``quantize_tiles``: per 128-row tile, scale = amax / 448 and codes =
-  e4m3_round(x / scale); dequantized value = code * scale.
+  e4m3_round(x * (448 / amax)); dequantized value = code * scale.  (The page
+  fixes one scale per tile; how a value becomes a code it leaves open: the
+  reading here maps the tile's amax onto E4M3's largest value 448.)
 
 ``attention_on_codes`` is the attention the FP8 path approximates: the exact
 definition (``oracle.fwd``, fp64) applied to the dequantized codes.  The kernel
@@ -130,26 +132,34 @@ def _scale_of(amax):
     return np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
 
 
+def _factor_of(amax):
+    """fp32 factor 448 / amax that maps the tile onto E4M3's range, 1 where amax is 0."""
+    amax = np.asarray(amax, np.float32)
+    safe = np.where(amax > 0, amax, np.float32(1.0)).astype(np.float32)
+    return np.where(amax > 0, np.float32(E4M3_MAX) / safe, np.float32(1.0)).astype(np.float32)
+
+
 def quantize_tiles(x: np.ndarray, tile: int = 128, per_tensor: bool = False):
     """Per-tile scale and E4M3 codes of x [BH, N, d] in float32 arithmetic:
-    amax over the tile's rows (rows past N count as 0), scale = amax / 448 (1
-    when the tile is all zero), code = e4m3(x / scale).  per_tensor: amax over
-    the whole tensor instead, the same scale for every tile.
+    amax over the tile's rows (rows past N count as 0), scale = amax / 448 and
+    code = e4m3(x * (448 / amax)) (scale and factor 1 when the tile is all
+    zero), so that code * scale ~ x.  per_tensor: amax over the whole tensor
+    instead, the same scale for every tile.
     Returns (codes uint8 [BH, N, d], scales float32 [BH, ceil(N/tile)])."""
     x = np.asarray(x, np.float32)
     BH, N, d = x.shape
     nt = (N + tile - 1) // tile
     scales = np.ones((BH, nt), np.float32)
     codes = np.zeros((BH, N, d), np.uint8)
-    whole = _scale_of(np.abs(x).max()) if per_tensor else None
+    whole = np.abs(x).max() if per_tensor else None
     for t in range(nt):
         blk = x[:, t * tile:(t + 1) * tile, :]
         if per_tensor:
-            sc = np.full(BH, whole, np.float32)
+            amax = np.full(BH, whole, np.float32)
         else:
-            sc = _scale_of(np.abs(blk).reshape(BH, -1).max(axis=1))
-        scales[:, t] = sc
-        y = (blk / sc[:, None, None]).astype(np.float32)
+            amax = np.abs(blk).reshape(BH, -1).max(axis=1).astype(np.float32)
+        scales[:, t] = _scale_of(amax)
+        y = (blk * _factor_of(amax)[:, None, None]).astype(np.float32)
         codes[:, t * tile:(t + 1) * tile, :] = e4m3_encode(e4m3_round(y))
     return codes, scales
 

@@ -35,10 +35,10 @@ def f32_of(t):
 
 
 def key_of_index(i):
-    """Key order of V^T within a 128-key tile (the layout fa.h documents)."""
-    e, c = i % 4, i // 4
-    h, w, x = c // 16, (c // 4) % 4, c % 4
-    return 64 * h + 32 * (e // 2) + 8 * w + 2 * x + e % 2
+    """Key order of V^T within a 128-key tile (the layout fa.h documents):
+    i = 64 h + 16 x + 2 w + e holds key 64 h + 8 w + 2 x + e."""
+    h, x, w, e = i // 64, (i // 16) % 4, (i // 2) % 8, i % 2
+    return 64 * h + 8 * w + 2 * x + e
 
 
 PERM = np.array([key_of_index(i) for i in range(128)])

@@ -41,7 +41,8 @@ def fwd_flops(w, causal=True):
 
 KERNEL_SOURCES = {"fa_bwd_dkdv_kernel<128>": ("fa_bwd.cu", "ptx.cuh", "fa_internal.cuh"),
                   "fa_bwd_dq_kernel<128>": ("fa_bwd_dq.cu", "ptx.cuh", "fa_internal.cuh"),
-                  "fa_fwd_kernel<128>": ("fa_fwd.cu", "ptx.cuh", "fa_internal.cuh")}
+                  "fa_fwd_kernel<128>": ("fa_fwd.cu", "ptx.cuh", "fa_internal.cuh"),
+                  "fa_fwd_fp8_kernel": ("fa_fp8.cu", "ptx.cuh", "fa_internal.cuh")}
 
 
 def profiled_traffic(kernel):
@@ -500,7 +501,10 @@ def fp8_forward_timing(fa, wl, wg, gin, dev, stream, peak_bf16, reps=50):
     flops = fwd_flops(wg)
     tf = flops / (t_attn / 1e3) / 1e12
     peak_fp8 = 2.0 * peak_bf16
+    alg_bytes = B * H * (3 * N * wg.d + 2 * N * wg.d + 4 * N)  # Q8, K8, V8^T in, O bf16 + lse out
     return {"workload": f"fwd B={B} H={H} N={N} d={wg.d} K x3 causal, Q/K rotated, per-tile E4M3 scales",
+            "kernel": "fa_fwd_fp8_kernel", "algorithmic_bytes": alg_bytes,
+            "traffic": profiled_traffic("fa_fwd_fp8_kernel"),
             "attention_ms_median": t_attn, "quantize_ms_median": t_quant,
             "tflops": tf, "tflops_incl_quantize": flops / ((t_attn + t_quant) / 1e3) / 1e12,
             "pct_of_fp8_peak": 100.0 * tf / peak_fp8,

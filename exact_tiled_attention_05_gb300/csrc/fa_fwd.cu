@@ -9,12 +9,15 @@
 //   warp 1       MMA issuer (and TMEM allocation): S_t = Q_t K_j^T and
 //                O_t += P_t V_j on the tcgen05 tensor cores, accumulators in
 //                tensor memory (TMEM).
-//   warps 2-17   softmax, two threads per query row (16 warps: 2 tiles x 2
-//                column halves x 4 warps): each reads half of its S row from
-//                TMEM, applies the causal/tail mask, swaps the partial row max
-//                with its partner through shared memory, runs the online-softmax
-//                update, writes its half of P (bf16) back into TMEM over S, and
-//                at the end normalises its half of O and writes O and lse.
+//   warps 2-17   softmax (8 warps per Q tile): with the 16x256b TMEM shape a
+//                lane holds 32 scores of each of two rows (r and r + 8), and the
+//                four lanes of a quad together hold both rows in full, so a row
+//                max is a 3-input max chain plus two shuffles.  Each warp applies
+//                the causal/tail mask, runs the online-softmax update and writes
+//                P (bf16) back into TMEM over S in two parts (keys 0-63, then
+//                64-127), each handed to the MMA warp as soon as it is stored.
+//                At the end it normalises O into the tile's Q buffer, which the
+//                producer warp writes out with TMA, and writes lse.
 //
 // Online softmax ("07 GPU、资源估算与 FlashAttention" §7.8; "CS336 Lecture 5
 // notes" §11.3-§11.4): per row a running max m (log2 units of the scaled
@@ -35,18 +38,19 @@ using namespace ptx;
 
 constexpr int kBM = 128;        // query rows per Q tile
 constexpr int kBN = 128;        // keys per K/V tile
-constexpr int kThreads = 576;   // 18 warps: TMA, MMA (+TMEM allocation), 2 tiles x 2 halves x 4 softmax
+constexpr int kThreads = 576;   // 18 warps: TMA, MMA (+TMEM allocation), 2 tiles x 8 softmax
 constexpr int kFirstSoftmaxWarp = 2;
-constexpr int kSoftmaxPerTile = 256;  // threads per Q tile: two per query row
+constexpr int kSoftmaxPerTile = 256;  // threads per Q tile: a quad per pair of rows
 constexpr int kBoxBytes = 128 * 64 * 2;  // one TMA box: 128 rows x 64 bf16
 // Conditional rescaling ("FlashAttention 1–4" §"FlashAttention-4"): the
 // reference max m only moves when a tile's max exceeds it by more than 8 (log2
 // units, a factor 256), so most tiles skip the O rescale pass.  P = 2^(s - m)
 // then lies in [0, 256] and its largest entry is no longer exactly 1.0, so the
-// bf16 rounding of P would bias O on rows close to one-hot.  Two row sums fix
-// that: O is normalised by the sum of the bf16 weights the MMA actually used
-// (the rounding of the dominant weight cancels in the ratio), and lse uses the
-// fp32 sum of the unrounded weights.
+// bf16 rounding of P would bias O on rows close to one-hot.  The fix: per tile,
+// the difference between the bf16 and the fp32 value of the row's largest
+// weight is added to a correction lc, and O is normalised by l + lc (the
+// rounding of the dominant weight cancels in the ratio), while lse uses the
+// fp32 sum l of the unrounded weights.
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 // Software exp2 for a fraction of the elements ("FlashAttention 1–4"

@@ -211,7 +211,7 @@ _HALF_SUB_STEP = 2.0 ** -10
 P_SCALE = 16.0
 
 
-def p_rounding_bound(quant, scale: float, causal: bool, tile: int = 128):
+def p_rounding_bound(quant, scale: float, causal: bool, tile: int = 128, rows=None):
     """Per output element, the largest |O_fp8 - O_codes| that rounding P to
     E4M3 can cause, O_codes = ``attention_on_codes``.
 
@@ -222,24 +222,31 @@ def p_rounding_bound(quant, scale: float, causal: bool, tile: int = 128):
     The row sum l = sum p_k is corrected by the rounding of the largest weight
     of every tile, |lc| <= LC = sum_j max(2^-4 max_j p, 2^-10 / c_j), so
         |O_fp8 - O_codes| <= (sum_k |dP_k| |v_k| + |O_codes| LC) / (l - LC).
-    Returns (bound [BH, N, d], o_codes [BH, N, d])."""
+    rows: optional int array [BH, R] of query rows to evaluate (all rows when
+    None).  Returns (bound, o_codes, lse_codes), [BH, R, d], [BH, R, d], [BH, R]."""
     qd, kd, vd = dequantized_qkv(quant, tile)
     sv = quant["v"][1].astype(np.float64)
     BH, N, d = qd.shape
     c = P_SCALE * sv / sv.max(axis=1, keepdims=True)            # [BH, T]
     key_tile = np.arange(N) // tile
-    bound = np.empty((BH, N, d))
-    o_ref = np.empty((BH, N, d))
+    if rows is None:
+        rows = np.tile(np.arange(N), (BH, 1))
+    rows = np.asarray(rows, np.int64)
+    R = rows.shape[1]
+    bound = np.empty((BH, R, d))
+    o_ref = np.empty((BH, R, d))
+    lse = np.empty((BH, R))
     for b in range(BH):
-        s = scale * (qd[b] @ kd[b].T)
+        s = scale * (qd[b][rows[b]] @ kd[b].T)                   # [R, N]
         if causal:
-            s = np.where(np.arange(N)[None, :] <= np.arange(N)[:, None], s, -np.inf)
-        p = np.exp(s - s.max(axis=1, keepdims=True))
+            s = np.where(np.arange(N)[None, :] <= rows[b][:, None], s, -np.inf)
+        m = s.max(axis=1, keepdims=True)
+        p = np.exp(s - m)
         l = p.sum(axis=1)
         ck = c[b][key_tile]                                      # [N] per key
         dp = np.maximum(_HALF_ULP_REL * p, _HALF_SUB_STEP / ck[None, :])
         dp = np.where(p > 0, dp, 0.0)                            # masked keys carry no weight
-        lc = np.zeros(N)
+        lc = np.zeros(R)
         for j in range(c.shape[1]):
             cols = key_tile == j
             pj = p[:, cols]
@@ -248,5 +255,6 @@ def p_rounding_bound(quant, scale: float, causal: bool, tile: int = 128):
                                            _HALF_SUB_STEP / c[b, j]), 0.0)
         o = (p @ vd[b]) / l[:, None]
         o_ref[b] = o
+        lse[b] = m[:, 0] + np.log(l)
         bound[b] = (dp @ np.abs(vd[b]) + np.abs(o) * lc[:, None]) / (l - lc)[:, None]
-    return bound, o_ref
+    return bound, o_ref, lse

@@ -126,7 +126,7 @@ def test_fp8_forward_parity(B, H, N, causal, rotate, per_tensor):
     scale = 1.0 / math.sqrt(D)
     inp, words, o, lse = fp8_case(B, H, N, causal, rotate, per_tensor, seed=N)
     quant = oracle_quant(inp, words, rotate, per_tensor)
-    bound, o_ref = ofp8.p_rounding_bound(quant, scale, causal)
+    bound, o_ref, _ = ofp8.p_rounding_bound(quant, scale, causal)
     _, lse_ref = ofp8.attention_on_codes(quant, scale, causal)
     # rounding of the bf16 output, plus fp32 scores / ex2 (relative 1e-4 of the
     # bound's scale is far above their ~1e-6)
@@ -140,6 +140,40 @@ def test_fp8_forward_parity(B, H, N, causal, rotate, per_tensor):
     # the bound is a worst case; the typical error must sit well inside it
     assert err.mean() <= 0.5 * bound.mean() + 1e-6
     check_lse(lse, lse_ref, f"fp8 lse B={B} H={H} N={N} causal={causal}")
+
+
+def test_fp8_full_size_sampled_rows():
+    """The workload and launch the bench times (B=2 H=16 N=8192 d=128, K x3,
+    causal, rotation on, per-tile scales): codes and scales bit-exact in full,
+    O within the P-rounding bound and lse within 1e-3 on 64 sampled query rows
+    per head (rows 0 and N-1 included)."""
+    w = wl.WORKLOADS["fwd_8k_d128_kx3"]
+    inp = wl.make_inputs(w)
+    words = wl.sign_bits(w.seed + 7)
+    q, k, v = (inp[n].to(DEV) for n in ("q", "k", "v"))
+    ws = fa.quantize_fp8(q, k, v, signs=words)
+    o, lse = fa.forward_fp8_quantized(ws, w.B, w.H, w.N, causal=True)
+    fa.sync_status()
+    views = {n: t.cpu().numpy() for n, t in fa.fp8_workspace_views(ws, w.B, w.H, w.N).items()}
+    del q, k, v, ws
+    quant = oracle_quant(inp, words, True, False)
+    assert np.array_equal(views["q8"], quant["q"][0]) and np.array_equal(views["k8"], quant["k"][0])
+    for name, key in (("sq", "q"), ("sk", "k"), ("sv", "v")):
+        assert np.array_equal(views[name].view(np.uint32), quant[key][1].view(np.uint32))
+    T = w.N // 128
+    vt = views["vt8"].reshape(w.BH, D, T, 128).transpose(0, 2, 3, 1)
+    assert np.array_equal(vt[:, :, np.argsort(PERM), :].reshape(w.BH, w.N, D), quant["v"][0])
+    rows = wl.sampled_rows(w, count=64)
+    bound, o_ref, lse_ref = ofp8.p_rounding_bound(quant, w.scale, True, rows=rows)
+    o = to_np(o).reshape(w.BH, w.N, D)
+    lse = to_np(lse).reshape(w.BH, w.N)
+    got = np.stack([o[b][rows[b]] for b in range(w.BH)])
+    got_l = np.stack([lse[b][rows[b]] for b in range(w.BH)])
+    err = np.abs(got - o_ref)
+    slack = bf16_half_ulp(o_ref) + 1e-4 * np.abs(o_ref) + 1e-6
+    assert (err - bound - slack).max() <= 0, f"max err {err.max():.3e}"
+    assert err.mean() <= 0.5 * bound.mean() + 1e-6
+    check_lse(got_l, lse_ref, "fp8 full size lse")
 
 
 def test_fp8_single_key_is_exact_value():

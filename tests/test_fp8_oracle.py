@@ -290,9 +290,16 @@ def test_p_rounding_bound_holds(N, causal, vscale):
     v = r.standard_normal((BH, N, d)).astype(np.float32)
     v[:, 128:] *= vscale                         # small V tiles: small fold, subnormal P
     quant = fp8.quantize_qkv(q, k, v, rotate=False)
-    bound, o_codes = fp8.p_rounding_bound(quant, 0.5, causal)
-    o_codes2, _ = fp8.attention_on_codes(quant, 0.5, causal)
+    bound, o_codes, lse_codes = fp8.p_rounding_bound(quant, 0.5, causal)
+    o_codes2, lse2 = fp8.attention_on_codes(quant, 0.5, causal)
     assert np.abs(o_codes - o_codes2).max() < 1e-12
+    assert np.abs(lse_codes - lse2).max() < 1e-12
+    rows = np.array([[0, 7, N - 1], [1, N // 2, N - 2]])
+    b_s, o_s, l_s = fp8.p_rounding_bound(quant, 0.5, causal, rows=rows)
+    for h in range(2):
+        assert np.abs(o_s[h] - o_codes[h][rows[h]]).max() < 1e-12
+        assert np.abs(b_s[h] - bound[h][rows[h]]).max() < 1e-12
+        assert np.abs(l_s[h] - lse_codes[h][rows[h]]).max() < 1e-12
     em = emulate_p_rounding(quant, 0.5, causal)
     err = np.abs(em - o_codes)
     assert np.all(err <= bound * (1 + 1e-9) + 1e-15)

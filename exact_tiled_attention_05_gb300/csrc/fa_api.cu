@@ -62,10 +62,15 @@ int floor_pow2(int x) {
     return p;
 }
 
-// Checks the current device (sm_103) and returns its status-word address.
+// Checks the current device (sm_103) and returns its status-word address.  It
+// also makes the device's primary context current on the calling thread: the
+// tensor-map encoding is a driver call that needs a current context, and a
+// thread that has made no runtime call yet (a worker thread, for example) has
+// none.
 int device_ready(int** status_out) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return kErrCuda;
+    if (cudaSetDevice(dev) != cudaSuccess) return kErrCuda;
     if (dev >= kMaxDevices) return kErrUnsupported;
     DeviceState& st = g_dev[dev];
     int c = st.checked.load(std::memory_order_acquire);

@@ -148,3 +148,43 @@ def test_autograd_wrapper_matches_oracle():
     assert err.max() <= 1e-2 and err.mean() <= 1e-3
     for got, ref, name in ((q.grad, g[0], "dq"), (k.grad, g[1], "dk"), (v.grad, g[2], "dv")):
         check_grad(to_np(got).reshape(ref.shape), ref, f"autograd {name}")
+
+
+def test_entry_points_from_a_fresh_host_thread():
+    """Every entry point called first on a thread that has made no CUDA call
+    (autograd runs the backward on such a worker thread): the library makes
+    the device's context current itself before encoding its tensor maps."""
+    import threading
+    B, H, N, d = 1, 2, 333, 128
+    inp = small_inputs(B, H, N, d, seed=78)
+    q, k, v, do = (inp[n].to(DEV) for n in ("q", "k", "v", "do"))
+    o_ref, lse_ref = fa.forward(q, k, v, causal=True)
+    g_ref = fa.backward(q, k, v, o_ref, lse_ref, do, causal=True)
+    words = wl.sign_bits(5)
+    o8_ref = fa.forward_fp8(q, k, v, signs=words, causal=True)[0]
+    fa.sync_status()
+    torch.cuda.synchronize()
+    out = {}
+
+    def work(name):
+        try:
+            if name == "fwd":
+                out[name] = fa.forward(q, k, v, causal=True)
+            elif name == "bwd":
+                out[name] = fa.backward(q, k, v, o_ref, lse_ref, do, causal=True)
+            else:
+                out[name] = fa.forward_fp8(q, k, v, signs=words, causal=True)
+            torch.cuda.synchronize()
+        except Exception as e:  # reported below, in the test's own thread
+            out[name] = e
+
+    for name in ("fwd", "bwd", "fp8"):
+        t = threading.Thread(target=work, args=(name,))
+        t.start()
+        t.join()
+        assert not isinstance(out[name], Exception), f"{name}: {out[name]!r}"
+    fa.sync_status()
+    assert torch.equal(out["fwd"][0], o_ref) and torch.equal(out["fwd"][1], lse_ref)
+    for a_, b_ in zip(out["bwd"], g_ref):
+        assert torch.equal(a_, b_)
+    assert torch.equal(out["fp8"][0], o8_ref)

@@ -403,19 +403,35 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                 reg_fence(r1);
                 const uint32_t lse_addr = smem_u32(&sm.lse2[qs][wg * 64]);
                 const bool diag = a.causal && i == j;
+                // only the diagonal tile and key rows past the end need a mask
+                const bool masked = diag || !row_valid;
 #pragma unroll
                 for (int part = 0; part < 2; ++part) {
+                    if (masked) {
 #pragma unroll
-                    for (int c4 = 0; c4 < 8; ++c4) {
-                        const float4 l4 = ld_shared_f4(lse_addr + (part * 8 + c4) * 16);
-                        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+                        for (int c4 = 0; c4 < 8; ++c4) {
+                            const float4 l4 = ld_shared_f4(lse_addr + (part * 8 + c4) * 16);
+                            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int c = part * 32 + c4 * 4 + e;
-                            const float sv = __uint_as_float(part == 0 ? r0[c] : r1[c - 32]);
-                            p[c] = ex2(fmaf(sv, sl2, -lv[e]));
-                            // rows past the end, and on the diagonal tile queries before the key
-                            if (!row_valid || (diag && wg * 64 + c < row)) p[c] = 0.f;
+                            for (int e = 0; e < 4; ++e) {
+                                const int c = part * 32 + c4 * 4 + e;
+                                const float sv = __uint_as_float(part == 0 ? r0[c] : r1[c - 32]);
+                                p[c] = ex2(fmaf(sv, sl2, -lv[e]));
+                                // rows past the end, and on the diagonal tile queries before the key
+                                if (!row_valid || wg * 64 + c < row) p[c] = 0.f;
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int c4 = 0; c4 < 8; ++c4) {
+                            const float4 l4 = ld_shared_f4(lse_addr + (part * 8 + c4) * 16);
+                            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int c = part * 32 + c4 * 4 + e;
+                                const float sv = __uint_as_float(part == 0 ? r0[c] : r1[c - 32]);
+                                p[c] = ex2(fmaf(sv, sl2, -lv[e]));
+                            }
                         }
                     }
                     uint32_t pk[16];

@@ -215,7 +215,7 @@ int bwd_common(BwdArgs& a, int B, int H, int N, int d, float scale, int causal, 
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return kErrWorkspace;
     if (workspace_bytes < ws_bytes(B, H, N)) return kErrWorkspace;
     a.delta = static_cast<float*>(workspace);
-    a.lse2 = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + ws_half(B, H, N));
+    a.nlse2 = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + ws_half(B, H, N));
     a.BH = B * H;
     a.N = N;
     a.n_kblk = (N + 127) / 128;

@@ -8,10 +8,11 @@ namespace {
 using namespace ptx;
 
 // ---------------------------------------------------------------------------
-// prep: D_i = sum_c dO[i,c] * O[i,c] (fp32) and lse_i * log2(e), d/8 threads
-// per row (one 16-byte vector of O and of dO each), written for every row of
-// whole 128-row tiles so that the two kernels after it load a tile's 128
-// values with one bulk copy; padding rows get D = 0 and lse * log2(e) = +inf.
+// prep: D_i = sum_c dO[i,c] * O[i,c] (fp32) and -lse_i * log2(e) (negated, so
+// that the exponent of P is one fused multiply-add), d/8 threads per row (one
+// 16-byte vector of O and of dO each), written for every row of whole 128-row
+// tiles so that the two kernels after it load a tile's 128 values with one bulk
+// copy; padding rows get D = 0 and -lse * log2(e) = -inf.
 // ---------------------------------------------------------------------------
 template <int HD>
 __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const BwdArgs a) {
@@ -37,11 +38,11 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const BwdArgs a) {
             real[u] = rp[u] < rows && i < a.N;
             const long long r = bh * a.N + i;
             ov[u] = dv[u] = make_uint4(0u, 0u, 0u, 0u);
-            lv[u] = INFINITY;
+            lv[u] = -INFINITY;
             if (real[u]) {
                 ov[u] = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.o) + r * HD) + sub);
                 dv[u] = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.dout) + r * HD) + sub);
-                if (sub == 0) lv[u] = __ldg(a.lse + r) * 1.4426950408889634f;
+                if (sub == 0) lv[u] = __ldg(a.lse + r) * -1.4426950408889634f;
             }
         }
 #pragma unroll
@@ -58,7 +59,7 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const BwdArgs a) {
             for (int off = kTPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
             if (sub == 0 && rp[u] < rows) {
                 a.delta[rp[u]] = real[u] ? acc : 0.f;
-                a.lse2[rp[u]] = lv[u];  // +inf for padding rows
+                a.nlse2[rp[u]] = lv[u];  // -inf for padding rows
             }
         }
     }
@@ -115,7 +116,7 @@ struct alignas(1024) BwdSmem {
     uint8_t v[BwdCfg<HD>::kTile];
     uint8_t q[BwdCfg<HD>::kQSlots][BwdCfg<HD>::kTile];
     uint8_t dout[BwdCfg<HD>::kDoSlots][BwdCfg<HD>::kTile];
-    float lse2[BwdCfg<HD>::kQSlots][128];    // with the Q slot
+    float nlse2[BwdCfg<HD>::kQSlots][128];   // -lse * log2(e), with the Q slot
     float delta[BwdCfg<HD>::kDoSlots][128];  // with the dO slot
     uint64_t kv_full;
     uint64_t q_full[BwdCfg<HD>::kQSlots];    // Q tile and its lse * log2(e) landed
@@ -246,7 +247,7 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                 mbar_arrive_expect_tx(qbar, Cfg::kTile + 512);
                 for (int b = 0; b < Cfg::kBoxes; ++b)
                     tma_load_3d(smem_u32(sm.q[qs] + b * kBBox), &tq, qbar, b * 64, i * 128, bh);
-                bulk_load(smem_u32(sm.lse2[qs]), a.lse2 + stat_row + i * 128, 512, qbar);
+                bulk_load(smem_u32(sm.nlse2[qs]), a.nlse2 + stat_row + i * 128, 512, qbar);
                 ++issued_q;
             }
             const int ds = it % Cfg::kDoSlots;
@@ -401,7 +402,8 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                 tmem_wait_ld();
                 reg_fence(r0);
                 reg_fence(r1);
-                const uint32_t lse_addr = smem_u32(&sm.lse2[qs][wg * 64]);
+                const uint32_t lse_addr = smem_u32(&sm.nlse2[qs][wg * 64]);
+                const uint64_t sl2_pair = f2_pack(sl2, sl2);
                 const bool diag = a.causal && i == j;
                 // only the diagonal tile and key rows past the end need a mask
                 const bool masked = diag || !row_valid;
@@ -411,26 +413,31 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
 #pragma unroll
                         for (int c4 = 0; c4 < 8; ++c4) {
                             const float4 l4 = ld_shared_f4(lse_addr + (part * 8 + c4) * 16);
-                            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+                            const uint64_t nl[2] = {f2_pack(l4.x, l4.y), f2_pack(l4.z, l4.w)};
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) {
+                            for (int e = 0; e < 4; e += 2) {
                                 const int c = part * 32 + c4 * 4 + e;
-                                const float sv = __uint_as_float(part == 0 ? r0[c] : r1[c - 32]);
-                                p[c] = ex2(fmaf(sv, sl2, -lv[e]));
+                                const uint32_t s0 = part == 0 ? r0[c] : r1[c - 32], s1 = part == 0 ? r0[c + 1] : r1[c - 31];
+                                const float2 x = f2_unpack(f2_fma(f2_pack_u(s0, s1), sl2_pair, nl[e >> 1]));
+                                p[c] = ex2(x.x);
+                                p[c + 1] = ex2(x.y);
                                 // rows past the end, and on the diagonal tile queries before the key
                                 if (!row_valid || wg * 64 + c < row) p[c] = 0.f;
+                                if (!row_valid || wg * 64 + c + 1 < row) p[c + 1] = 0.f;
                             }
                         }
                     } else {
 #pragma unroll
                         for (int c4 = 0; c4 < 8; ++c4) {
                             const float4 l4 = ld_shared_f4(lse_addr + (part * 8 + c4) * 16);
-                            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+                            const uint64_t nl[2] = {f2_pack(l4.x, l4.y), f2_pack(l4.z, l4.w)};
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) {
+                            for (int e = 0; e < 4; e += 2) {
                                 const int c = part * 32 + c4 * 4 + e;
-                                const float sv = __uint_as_float(part == 0 ? r0[c] : r1[c - 32]);
-                                p[c] = ex2(fmaf(sv, sl2, -lv[e]));
+                                const uint32_t s0 = part == 0 ? r0[c] : r1[c - 32], s1 = part == 0 ? r0[c + 1] : r1[c - 31];
+                                const float2 x = f2_unpack(f2_fma(f2_pack_u(s0, s1), sl2_pair, nl[e >> 1]));
+                                p[c] = ex2(x.x);
+                                p[c + 1] = ex2(x.y);
                             }
                         }
                     }
@@ -461,15 +468,14 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
 #pragma unroll
                 for (int c4 = 0; c4 < 8; ++c4) {
                     const float4 d4 = ld_shared_f4(d_addr + (h * 32 + c4 * 4) * 4);
-                    const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
-                    float ds4[4];
+                    const uint64_t dd[2] = {f2_pack(d4.x, d4.y), f2_pack(d4.z, d4.w)};
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
+                    for (int e = 0; e < 4; e += 2) {
                         const int c = c4 * 4 + e;
-                        ds4[e] = p[h * 32 + c] * (__uint_as_float(r[c]) - dv[e]);
+                        const float2 ds = f2_unpack(f2_mul(f2_pack(p[h * 32 + c], p[h * 32 + c + 1]),
+                                                           f2_sub(f2_pack_u(r[c], r[c + 1]), dd[e >> 1])));
+                        pk[h * 16 + c4 * 2 + (e >> 1)] = pack_bf16x2(ds.x, ds.y);
                     }
-                    pk[h * 16 + c4 * 2] = pack_bf16x2(ds4[0], ds4[1]);
-                    pk[h * 16 + c4 * 2 + 1] = pack_bf16x2(ds4[2], ds4[3]);
                 }
             }
             // dS^T over the first 32 of the 64 dP^T columns this thread read

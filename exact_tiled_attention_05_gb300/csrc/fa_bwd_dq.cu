@@ -55,7 +55,7 @@ struct alignas(1024) DqSmem {
     uint8_t dout[DqCfg<HD>::kTile];
     uint8_t k[DqCfg<HD>::kKSlots][DqCfg<HD>::kTile];
     uint8_t v[DqCfg<HD>::kVSlots][DqCfg<HD>::kTile];
-    float lse2[128];   // lse * log2(e) per query row (+inf past the end)
+    float nlse2[128];  // -lse * log2(e) per query row (-inf past the end)
     float delta[128];  // D per query row
     uint64_t qd_full;  // Q, dO and their lse * log2(e), D landed
     uint64_t k_full[DqCfg<HD>::kKSlots];
@@ -161,10 +161,10 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 tma_load_3d(smem_u32(sm.q + b * kQBox), &tq, qbar, b * 64, q0, bh);
                 tma_load_3d(smem_u32(sm.dout + b * kQBox), &tdo, qbar, b * 64, q0, bh);
             }
-            // the tile's lse * log2(e) and D (rows past the end: +inf and 0,
+            // the tile's -lse * log2(e) and D (rows past the end: -inf and 0,
             // written by the prep stage)
             const size_t stat = static_cast<size_t>(bh) * nq * 128 + q0;
-            bulk_load(smem_u32(sm.lse2), a.lse2 + stat, 512, qbar);
+            bulk_load(smem_u32(sm.nlse2), a.nlse2 + stat, 512, qbar);
             bulk_load(smem_u32(sm.delta), a.delta + stat, 512, qbar);
             // K_j then V_j, each into its own ring
             const int n_loads = FA_FAULT_INJECT ? 0 : n;
@@ -287,8 +287,10 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         const uint32_t lane_addr = tbase + (static_cast<uint32_t>(wq * 32) << 16);
         const float sl2 = a.scale_log2;
         bool ok = mbar_wait_warp(smem_u32(&sm.qd_full), 0, kWaitTimeoutNs, abort);
-        const float lse2 = ok ? sm.lse2[row] : 0.f;
+        const float nlse2 = ok ? sm.nlse2[row] : 0.f;
         const float dval = ok ? sm.delta[row] : 0.f;
+        const uint64_t sl2_pair = f2_pack(sl2, sl2), nl_pair = f2_pack(nlse2, nlse2);
+        const uint64_t d_pair = f2_pack(dval, dval);
         for (int j = 0; ok && j < n; ++j) {
             const uint32_t dbuf = Cfg::kDP + static_cast<uint32_t>(j & 1) * 128 + half * 64;
             if (!(ok = mbar_wait_warp(smem_u32(&sm.s_full), j & 1, kWaitTimeoutNs, abort))) break;
@@ -304,8 +306,12 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 tc_fence_before();
                 mbar_arrive(smem_u32(&sm.s_free));
 #pragma unroll
-                for (int c = 0; c < 64; ++c)
-                    p[c] = ex2(fmaf(__uint_as_float(c < 32 ? r0[c] : r1[c - 32]), sl2, -lse2));
+                for (int c = 0; c < 64; c += 2) {
+                    const uint32_t s0 = c < 32 ? r0[c] : r1[c - 32], s1 = c < 32 ? r0[c + 1] : r1[c - 31];
+                    const float2 x = f2_unpack(f2_fma(f2_pack_u(s0, s1), sl2_pair, nl_pair));
+                    p[c] = ex2(x.x);
+                    p[c + 1] = ex2(x.y);
+                }
             }
             const int kbase = j * 128 + half * 64;
             if ((j * 128 + 128 > N) || (a.causal && j * 128 + 127 > q0)) {
@@ -327,8 +333,9 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
 #pragma unroll
                 for (int c = 0; c < 16; ++c) {
                     const int e = h * 32 + 2 * c;
-                    pk[h * 16 + c] = pack_bf16x2(p[e] * (__uint_as_float(r[2 * c]) - dval),
-                                                 p[e + 1] * (__uint_as_float(r[2 * c + 1]) - dval));
+                    const float2 ds = f2_unpack(f2_mul(f2_pack(p[e], p[e + 1]),
+                                                       f2_sub(f2_pack_u(r[2 * c], r[2 * c + 1]), d_pair)));
+                    pk[h * 16 + c] = pack_bf16x2(ds.x, ds.y);
                 }
             }
             // dS over the first 32 of the 64 dP columns this thread read

@@ -59,7 +59,7 @@ struct BwdArgs {
     void* dv;
     // workspace, fp32 [BH, n_kblk * 128] (rows padded to whole 128-row tiles):
     float* delta;     // D = rowsum(dO * O); 0 in the padding
-    float* lse2;      // lse * log2(e); +inf in the padding (P = 0 there)
+    float* nlse2;     // -lse * log2(e); -inf in the padding (P = 0 there)
     int BH;
     int N;
     int n_kblk;       // 128-row key blocks per head (= 128-row query blocks)

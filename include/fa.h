@@ -58,7 +58,7 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
            int B, int H, int N, int d, float scale, int causal, void* stream);
 
 /* Bytes of device workspace fa_bwd needs for these sizes: two fp32 row
- * statistics, D = rowsum(dO * O) and lse * log2(e), each [B*H, N rounded up to
+ * statistics, D = rowsum(dO * O) and -lse * log2(e), each [B*H, N rounded up to
  * a multiple of 128] and rounded up to 256 bytes (d does not change it). */
 size_t fa_bwd_workspace_size(int B, int H, int N, int d);
 
@@ -77,7 +77,7 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
            void* workspace, size_t workspace_bytes, void* stream);
 
 /* The three stages of fa_bwd, exposed so a caller can time or overlap them.
- * prep: D = rowsum(dO * O) and lse * log2(e) into the workspace.
+ * prep: D = rowsum(dO * O) and -lse * log2(e) into the workspace.
  * main: per key/value tile, recompute S and P = exp(S - lse) and accumulate
  *       dV and dK on chip; writes dk, dv.
  * dq:   per query tile, recompute S, P and dP = dO V^T and accumulate

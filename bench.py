@@ -452,6 +452,31 @@ def run_gpu(args, world, rank, local):
     check(fa.fa_sync_status(h), "fp8 forward")
 
     del gin, go, gl
+
+    # ---------------- forward at N = 32768 (the long-context workload), causal ----------------
+    wl32 = wl.WORKLOADS["fwd_32k_d128"]
+    lin = wl.make_inputs(wl32, device=dev)
+    lo = torch.empty_like(lin["q"])
+    ll = torch.empty(wl32.B, wl32.H, wl32.N, dtype=torch.float32, device=dev)
+    for _ in range(3):
+        fa.forward(lin["q"], lin["k"], lin["v"], causal=True, out=lo, lse=ll)
+    lreps = 10
+    le = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(lreps)]
+    torch.cuda.synchronize(dev)
+    for a_, b_ in le:
+        a_.record(stream)
+        fa.forward(lin["q"], lin["k"], lin["v"], causal=True, out=lo, lse=ll)
+        b_.record(stream)
+    torch.cuda.synchronize(dev)
+    check(fa.fa_sync_status(h), "forward 32k")
+    lms = sorted(a_.elapsed_time(b_) for a_, b_ in le)
+    f_long = fwd_flops(wl32) / (lms[lreps // 2] / 1e3) / 1e12
+    fwd_long = {"workload": f"fwd B={wl32.B} H={wl32.H} N={wl32.N} d={wl32.d} causal",
+                "ms_median": lms[lreps // 2], "tflops": f_long,
+                "pct_of_bf16_peak": 100.0 * f_long / peak_burst,
+                "gate": ">= 60% of dense BF16 peak"}
+    del lin, lo, ll
+
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
@@ -461,7 +486,7 @@ def run_gpu(args, world, rank, local):
         "peak_bf16_tflops": peak_burst, "peak_source": peak_src,
         "kernel_ms": per, "roofline": roofline, "e2e": e2e,
         "gpu_launches": 4 * args.steps,
-        "clocks": clk, "forward_gate": fwd_gate, "fp8_forward": fp8,
+        "clocks": clk, "forward_gate": fwd_gate, "forward_gate_long": fwd_long, "fp8_forward": fp8,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = oracle_baseline(w, cpu_in)

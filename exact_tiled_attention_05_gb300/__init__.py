@@ -108,7 +108,8 @@ def fa_bwd_dq(q, k, v, lse, dout, dq, B, H, N, d, scale, causal, ws, ws_bytes, s
 
 def fa_bwd_noalloc(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, causal, stream):
     """fa_bwd without a workspace argument, for callers that cannot allocate
-    device memory: the scratch is a fixed 64 MiB array inside the library."""
+    device memory: the scratch is a fixed array (64 MiB + 256 bytes) inside the
+    library."""
     return load_library().fa_bwd_noalloc(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale,
                                          causal, stream)
 

@@ -150,7 +150,7 @@ size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 size_t ws_half(int B, int H, int N) {
     return round256(static_cast<size_t>(B) * H * ((N + 127) / 128) * 128 * sizeof(float));
 }
-size_t ws_bytes(int B, int H, int N) { return 2 * ws_half(B, H, N); }
+size_t ws_bytes(int B, int H, int N) { return 2 * ws_half(B, H, N) + 256; }  // + work counter
 
 // FP8 workspace: segment offsets (each 256-byte aligned), in the order fa.h lists.
 struct Fp8Layout {
@@ -216,6 +216,7 @@ int bwd_common(BwdArgs& a, int B, int H, int N, int d, float scale, int causal, 
     if (workspace_bytes < ws_bytes(B, H, N)) return kErrWorkspace;
     a.delta = static_cast<float*>(workspace);
     a.nlse2 = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + ws_half(B, H, N));
+    a.work = reinterpret_cast<unsigned*>(static_cast<uint8_t*>(workspace) + 2 * ws_half(B, H, N));
     a.BH = B * H;
     a.N = N;
     a.n_kblk = (N + 127) / 128;
@@ -227,6 +228,7 @@ int bwd_common(BwdArgs& a, int B, int H, int N, int d, float scale, int causal, 
     // kernel: about two waves, as the forward
     a.group = clampi(floor_pow2(clampi((current_sms() * 9 / 10) / a.n_kblk, 1, 1 << 20)), 1, a.BH);
     a.group_dq = clampi(floor_pow2(clampi((2 * current_sms()) / a.n_kblk, 1, 1 << 20)), 1, a.BH);
+    a.sms = current_sms();
     a.scale = scale;
     a.scale_log2 = scale * 1.4426950408889634f;
     return kOk;

@@ -118,14 +118,17 @@ struct alignas(1024) BwdSmem {
     uint8_t dout[BwdCfg<HD>::kDoSlots][BwdCfg<HD>::kTile];
     float nlse2[BwdCfg<HD>::kQSlots][128];   // -lse * log2(e), with the Q slot
     float delta[BwdCfg<HD>::kDoSlots][128];  // with the dO slot
-    uint64_t kv_full;
+    int item[2];                             // work items published by the loader (-1: none left)
+    uint64_t item_full[2], item_empty[2];    // per queue slot: written / read by every role
+    uint64_t kv_full;                        // K_j and V_j of the item landed (once per item)
+    uint64_t k_free, v_free;                 // staged dK / dV read out of the K / V buffer (per item)
     uint64_t q_full[BwdCfg<HD>::kQSlots];    // Q tile and its lse * log2(e) landed
     uint64_t q_empty[BwdCfg<HD>::kQSlots];   // committed after dK(i)
     uint64_t do_full[BwdCfg<HD>::kDoSlots];  // dO tile and its D landed
     uint64_t do_empty[BwdCfg<HD>::kDoSlots]; // committed after dV(i)
     uint64_t p_ready[2];  // P^T for each thread's queries 0-31, then 32-63
     uint64_t s_full, dp_full, ds_ready, dkdv_done, drain;
-    uint64_t out_staged;  // every compute thread has staged its dV / dK row
+    uint64_t out_staged;  // every compute thread has staged its dV / dK row (per item)
     uint32_t tmem_base;
     int abort;
 };
@@ -141,6 +144,32 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
         "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
         "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
         : "memory");
+}
+
+// Work item t (launch order) -> (head, key block).  Causal: groups of a.group
+// heads; inside a group the key blocks with the most query tiles (small j)
+// come first.  Keeping few heads in flight keeps their Q and dO in L2.
+__device__ __forceinline__ void dkdv_item(const BwdArgs& a, int t, int& bh, int& j) {
+    if (a.causal) {
+        const int grp = t / (a.group * a.n_kblk);
+        const int first = grp * a.group;
+        const int gc = min(a.group, a.BH - first);
+        const int r = t - grp * a.group * a.n_kblk;
+        j = r / gc;
+        bh = first + r % gc;
+    } else {
+        bh = t / a.n_kblk;
+        j = t % a.n_kblk;
+    }
+}
+
+constexpr int kItemReaders = 2 + kBCompute;  // MMA thread, store thread, compute threads
+
+// Waits until at most N of this thread's committed bulk groups are still
+// reading their shared-memory source.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
 }
 
 __device__ __forceinline__ void bwd_timeout(const BwdArgs& a, volatile int* abort) {
@@ -166,28 +195,17 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     const int lane = threadIdx.x & 31;
     const int N = a.N;
     const int nq = a.n_kblk;  // query tiles == key tiles (both 128 rows)
-    int bh, j;
-    if (a.causal) {
-        // groups of a.group heads; inside a group the key blocks with the most
-        // query tiles (small j) launch first.  Keeping few heads in flight keeps
-        // their Q and dO resident in L2.
-        const int b = static_cast<int>(blockIdx.x);
-        const int grp = b / (a.group * a.n_kblk);
-        const int first = grp * a.group;
-        const int gc = min(a.group, a.BH - first);
-        const int r = b - grp * a.group * a.n_kblk;
-        j = r / gc;
-        bh = first + r % gc;
-    } else {
-        bh = static_cast<int>(blockIdx.x) / a.n_kblk;
-        j = static_cast<int>(blockIdx.x) % a.n_kblk;
-    }
-    const int i_begin = a.causal ? j : 0;
-    const int niter = nq - i_begin;
+    const int n_items = a.BH * nq;
 
     if (threadIdx.x == 0) {
         sm.abort = 0;
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(smem_u32(&sm.item_full[s]), 1);
+            mbar_init(smem_u32(&sm.item_empty[s]), kItemReaders);
+        }
         mbar_init(smem_u32(&sm.kv_full), 1);
+        mbar_init(smem_u32(&sm.k_free), 1);
+        mbar_init(smem_u32(&sm.v_free), 1);
         for (int s = 0; s < Cfg::kQSlots; ++s) {
             mbar_init(smem_u32(&sm.q_full[s]), 1);
             mbar_init(smem_u32(&sm.q_empty[s]), 1);
@@ -217,55 +235,71 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
 
     if (warp == 0) {
         // ===================== loads =====================
-        const bool leader = lane == 0;
-        if (leader) {
+        // Per item: fetch its index and publish it to the other roles; then the
+        // first query tile's Q and dO, K_j and V_j (their buffers hold the previous
+        // item's staged dK / dV until the store warp has read them), and the
+        // remaining query tiles.  Q and dO use rings indexed by the CTA's running
+        // tile count g, so one item's tiles follow the previous item's.
+        if (lane == 0) {
             tma_prefetch_desc(&tq);
             tma_prefetch_desc(&tk);
             tma_prefetch_desc(&tv);
             tma_prefetch_desc(&tdo);
-            const uint32_t bar = smem_u32(&sm.kv_full);
-            mbar_arrive_expect_tx(bar, 2 * Cfg::kTile);
-            for (int b = 0; b < Cfg::kBoxes; ++b) {
-                tma_load_3d(smem_u32(sm.k + b * kBBox), &tk, bar, b * 64, j * 128, bh);
-                tma_load_3d(smem_u32(sm.v + b * kBBox), &tv, bar, b * 64, j * 128, bh);
-            }
-        }
-        // Per query tile: the Q tile with its 128 values of lse * log2(e), then the
-        // dO tile with its 128 values of D (padded rows prepared by the prep stage).
-        const size_t stat_row = static_cast<size_t>(bh) * nq * 128;
-        int issued_q = 0, issued_do = 0;
-        for (int it = 0; leader && it < niter; ++it) {
-            const int i = i_begin + it;
-            const int qs = it % Cfg::kQSlots;
-            if (!mbar_wait(smem_u32(&sm.q_empty[qs]), ((it / Cfg::kQSlots) & 1) ^ 1, kWaitTimeoutNs,
-                           abort)) {
-                bwd_timeout(a, abort);
-                break;
-            }
-            if (!FA_FAULT_INJECT) {
+            int issued_q = 0, issued_do = 0, issued_kv = 0;
+            bool ok = true;
+            auto load_tile = [&](int bh, int i) -> bool {
+                const size_t stat = (static_cast<size_t>(bh) * nq + i) * 128;
+                const int qs = issued_q % Cfg::kQSlots;
+                if (!mbar_wait(smem_u32(&sm.q_empty[qs]), ((issued_q / Cfg::kQSlots) & 1) ^ 1,
+                               kWaitTimeoutNs, abort))
+                    return false;
+                if (FA_FAULT_INJECT) return true;
                 const uint32_t qbar = smem_u32(&sm.q_full[qs]);
                 mbar_arrive_expect_tx(qbar, Cfg::kTile + 512);
                 for (int b = 0; b < Cfg::kBoxes; ++b)
                     tma_load_3d(smem_u32(sm.q[qs] + b * kBBox), &tq, qbar, b * 64, i * 128, bh);
-                bulk_load(smem_u32(sm.nlse2[qs]), a.nlse2 + stat_row + i * 128, 512, qbar);
+                bulk_load(smem_u32(sm.nlse2[qs]), a.nlse2 + stat, 512, qbar);
                 ++issued_q;
-            }
-            const int ds = it % Cfg::kDoSlots;
-            if (!mbar_wait(smem_u32(&sm.do_empty[ds]), ((it / Cfg::kDoSlots) & 1) ^ 1, kWaitTimeoutNs,
-                           abort)) {
-                bwd_timeout(a, abort);
-                break;
-            }
-            if (!FA_FAULT_INJECT) {
+                const int ds = issued_do % Cfg::kDoSlots;
+                if (!mbar_wait(smem_u32(&sm.do_empty[ds]), ((issued_do / Cfg::kDoSlots) & 1) ^ 1,
+                               kWaitTimeoutNs, abort))
+                    return false;
                 const uint32_t dbar = smem_u32(&sm.do_full[ds]);
                 mbar_arrive_expect_tx(dbar, Cfg::kTile + 512);
                 for (int b = 0; b < Cfg::kBoxes; ++b)
                     tma_load_3d(smem_u32(sm.dout[ds] + b * kBBox), &tdo, dbar, b * 64, i * 128, bh);
-                bulk_load(smem_u32(sm.delta[ds]), a.delta + stat_row + i * 128, 512, dbar);
+                bulk_load(smem_u32(sm.delta[ds]), a.delta + stat, 512, dbar);
                 ++issued_do;
+                return true;
+            };
+            for (int k = 0; ok; ++k) {
+                const int slot = k & 1;
+                if (k >= 2 && !(ok = mbar_wait(smem_u32(&sm.item_empty[slot]), ((k - 2) >> 1) & 1,
+                                               kWaitTimeoutNs, abort)))
+                    break;
+                const unsigned t = atomicAdd(a.work, 1u);
+                const int item = t < static_cast<unsigned>(n_items) ? static_cast<int>(t) : -1;
+                sm.item[slot] = item;
+                mbar_arrive(smem_u32(&sm.item_full[slot]));
+                if (item < 0) break;
+                int bh, j;
+                dkdv_item(a, item, bh, j);
+                const int i_begin = a.causal ? j : 0;
+                if (!(ok = load_tile(bh, i_begin))) break;
+                const uint32_t kvbar = smem_u32(&sm.kv_full);
+                if (k >= 1 && !(ok = mbar_wait(smem_u32(&sm.k_free), (k - 1) & 1, kWaitTimeoutNs, abort)))
+                    break;
+                mbar_arrive_expect_tx(kvbar, 2 * Cfg::kTile);
+                for (int b = 0; b < Cfg::kBoxes; ++b)
+                    tma_load_3d(smem_u32(sm.k + b * kBBox), &tk, kvbar, b * 64, j * 128, bh);
+                ++issued_kv;
+                if (k >= 1 && !(ok = mbar_wait(smem_u32(&sm.v_free), (k - 1) & 1, kWaitTimeoutNs, abort)))
+                    break;
+                for (int b = 0; b < Cfg::kBoxes; ++b)
+                    tma_load_3d(smem_u32(sm.v + b * kBBox), &tv, kvbar, b * 64, j * 128, bh);
+                for (int i = i_begin + 1; ok && i < nq; ++i) ok = load_tile(bh, i);
             }
-        }
-        if (leader) {
+            if (!ok) bwd_timeout(a, abort);
             // Let every copy that was issued land before the CTA can exit.
             for (int s = 0; s < Cfg::kQSlots && s < issued_q; ++s) {
                 const int last = s + Cfg::kQSlots * ((issued_q - 1 - s) / Cfg::kQSlots);
@@ -275,8 +309,8 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                 const int last = s + Cfg::kDoSlots * ((issued_do - 1 - s) / Cfg::kDoSlots);
                 mbar_wait_drain(smem_u32(&sm.do_full[s]), (last / Cfg::kDoSlots) & 1, kWaitTimeoutNs);
             }
+            if (issued_kv > 0) mbar_wait_drain(smem_u32(&sm.kv_full), (issued_kv - 1) & 1, kWaitTimeoutNs);
         }
-        if (leader) mbar_wait_drain(smem_u32(&sm.kv_full), 0, kWaitTimeoutNs);
     } else if (warp == 1) {
         // ===================== MMA issuer =====================
         if (elect_one()) {
@@ -302,92 +336,138 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                             id_kmn, (acc || kk > 0) ? 1u : 0u);
                 }
             };
-            bool ok = mbar_wait(smem_u32(&sm.kv_full), 0, kWaitTimeoutNs, abort);
-            // S^T(0); afterwards S^T(i+1) is issued inside iteration i
-            if (ok && (ok = mbar_wait(smem_u32(&sm.q_full[0]), 0, kWaitTimeoutNs, abort))) {
-                tc_fence_after();
-                gemm_kk(Cfg::kS, k_addr, smem_u32(sm.q[0]));
-                umma_commit(smem_u32(&sm.s_full));
-            }
-            for (int it = 0; ok && it < niter; ++it) {
-                const int qs = it % Cfg::kQSlots, ds = it % Cfg::kDoSlots;
-                const uint32_t q_addr = smem_u32(sm.q[qs]), do_addr = smem_u32(sm.dout[ds]);
-                // dP^T(i) over dS^T(i-1): dK(i-1), which read it, was issued before.
-                if (!(ok = mbar_wait(smem_u32(&sm.do_full[ds]), (it / Cfg::kDoSlots) & 1,
+            bool ok = true;
+            int g = 0;  // running query-tile count of this CTA (ring positions, barrier phases)
+            for (int k = 0; ok; ++k) {
+                const int slot = k & 1;
+                if (!(ok = mbar_wait(smem_u32(&sm.item_full[slot]), (k >> 1) & 1, kWaitTimeoutNs, abort)))
+                    break;
+                const int item = sm.item[slot];
+                mbar_arrive(smem_u32(&sm.item_empty[slot]));
+                if (item < 0) break;
+                int bh, j;
+                dkdv_item(a, item, bh, j);
+                const int niter = nq - (a.causal ? j : 0);
+                // K_j, V_j of this item; the previous item's MMAs have all been issued
+                // (one thread's MMAs run in order), so S^T(0) may overwrite its P^T
+                if (!(ok = mbar_wait(smem_u32(&sm.kv_full), k & 1, kWaitTimeoutNs, abort))) break;
+                // S^T(0); afterwards S^T(i+1) is issued inside iteration i
+                if (!(ok = mbar_wait(smem_u32(&sm.q_full[g % Cfg::kQSlots]), (g / Cfg::kQSlots) & 1,
                                      kWaitTimeoutNs, abort)))
                     break;
                 tc_fence_after();
-                gemm_kk(Cfg::kDP, v_addr, do_addr);
-                umma_commit(smem_u32(&sm.dp_full));
-                // dV += P^T dO in two parts: queries {0-31, 64-95} (k-steps 0, 1, 4, 5),
-                // each thread's first half of P^T, then {32-63, 96-127}
-                for (int part = 0; ok && part < 2; ++part) {
-                    if (!(ok = mbar_wait(smem_u32(&sm.p_ready[part]), it & 1, kWaitTimeoutNs, abort)))
-                        break;
-                    tc_fence_after();
-#pragma unroll
-                    for (int x = 0; x < 4; ++x) {
-                        const int kk = (x >> 1) * 4 + part * 2 + (x & 1);
-                        const uint32_t col = Cfg::kS + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
-                        umma_ts(tbase + Cfg::kDV, tbase + col,
-                                sdesc_sw128(do_addr + kk * 2048, kBBox, 1024), id_kmn,
-                                (it > 0 || part > 0 || x > 0) ? 1u : 0u);
-                    }
-                }
-                if (!ok) break;
-                umma_commit(smem_u32(&sm.do_empty[ds]));  // dO_i read
-                // S^T(i+1) over P^T(i): dV(i) was issued before it.
-                if (it + 1 < niter) {
-                    const int qs1 = (it + 1) % Cfg::kQSlots;
-                    if (!(ok = mbar_wait(smem_u32(&sm.q_full[qs1]), ((it + 1) / Cfg::kQSlots) & 1,
+                gemm_kk(Cfg::kS, k_addr, smem_u32(sm.q[g % Cfg::kQSlots]));
+                umma_commit(smem_u32(&sm.s_full));
+                for (int it = 0; ok && it < niter; ++it, ++g) {
+                    const int qs = g % Cfg::kQSlots, ds = g % Cfg::kDoSlots;
+                    const uint32_t q_addr = smem_u32(sm.q[qs]), do_addr = smem_u32(sm.dout[ds]);
+                    // dP^T(i) over dS^T(i-1): dK(i-1), which read it, was issued before.
+                    if (!(ok = mbar_wait(smem_u32(&sm.do_full[ds]), (g / Cfg::kDoSlots) & 1,
                                          kWaitTimeoutNs, abort)))
                         break;
                     tc_fence_after();
-                    gemm_kk(Cfg::kS, k_addr, smem_u32(sm.q[qs1]));
-                    umma_commit(smem_u32(&sm.s_full));
+                    gemm_kk(Cfg::kDP, v_addr, do_addr);
+                    umma_commit(smem_u32(&sm.dp_full));
+                    // dV += P^T dO in two parts: queries {0-31, 64-95} (k-steps 0, 1, 4, 5),
+                    // each thread's first half of P^T, then {32-63, 96-127}.  The first of
+                    // an item overwrites dV: the previous item's dV was read out of TMEM
+                    // before its stores, and those before this item's K_j could load.
+                    for (int part = 0; ok && part < 2; ++part) {
+                        if (!(ok = mbar_wait(smem_u32(&sm.p_ready[part]), g & 1, kWaitTimeoutNs, abort)))
+                            break;
+                        tc_fence_after();
+#pragma unroll
+                        for (int x = 0; x < 4; ++x) {
+                            const int kk = (x >> 1) * 4 + part * 2 + (x & 1);
+                            const uint32_t col = Cfg::kS + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
+                            umma_ts(tbase + Cfg::kDV, tbase + col,
+                                    sdesc_sw128(do_addr + kk * 2048, kBBox, 1024), id_kmn,
+                                    (it > 0 || part > 0 || x > 0) ? 1u : 0u);
+                        }
+                    }
+                    if (!ok) break;
+                    umma_commit(smem_u32(&sm.do_empty[ds]));  // dO_i read
+                    // S^T(i+1) over P^T(i): dV(i) was issued before it.
+                    if (it + 1 < niter) {
+                        const int qs1 = (g + 1) % Cfg::kQSlots;
+                        if (!(ok = mbar_wait(smem_u32(&sm.q_full[qs1]), ((g + 1) / Cfg::kQSlots) & 1,
+                                             kWaitTimeoutNs, abort)))
+                            break;
+                        tc_fence_after();
+                        gemm_kk(Cfg::kS, k_addr, smem_u32(sm.q[qs1]));
+                        umma_commit(smem_u32(&sm.s_full));
+                    }
+                    if (!(ok = mbar_wait(smem_u32(&sm.ds_ready), g & 1, kWaitTimeoutNs, abort))) break;
+                    tc_fence_after();
+                    gemm_tmem_a(Cfg::kDK, Cfg::kDP, q_addr, it > 0);  // dK += dS^T Q
+                    umma_commit(smem_u32(&sm.q_empty[qs]));            // Q_i read
                 }
-                if (!(ok = mbar_wait(smem_u32(&sm.ds_ready), it & 1, kWaitTimeoutNs, abort))) break;
-                tc_fence_after();
-                gemm_tmem_a(Cfg::kDK, Cfg::kDP, q_addr, it > 0);  // dK += dS^T Q
-                umma_commit(smem_u32(&sm.q_empty[qs]));            // Q_i read
+                if (ok) umma_commit(smem_u32(&sm.dkdv_done));  // this item's dK, dV complete
             }
             if (!ok) bwd_timeout(a, abort);
-            umma_commit(smem_u32(&sm.dkdv_done));
             // Every MMA (and every commit before it) completes before the CTA leaves.
             umma_commit(smem_u32(&sm.drain));
             mbar_wait_drain(smem_u32(&sm.drain), 0, kWaitTimeoutNs);
         }
     } else if (warp == 3) {
         // ===================== dK / dV stores =====================
+        // Per item: the staged dK (in the K buffer) and dV (in the V buffer) go out
+        // with TMA tile stores, as two bulk groups; each buffer is handed back to
+        // the loader as soon as its group has been read out of shared memory.
         if (elect_one()) {
             tma_prefetch_desc(&tdk);
             tma_prefetch_desc(&tdv);
-            if (mbar_wait(smem_u32(&sm.out_staged), 0, kWaitTimeoutNs, abort)) {
-                for (int b = 0; b < Cfg::kBoxes; ++b) {
-                    tma_store_3d(&tdv, smem_u32(sm.q[0]) + b * kBBox, b * 64, j * 128, bh);
-                    tma_store_3d(&tdk, smem_u32(sm.q[1]) + b * kBBox, b * 64, j * 128, bh);
-                }
+            bool ok = true;
+            for (int k = 0; ok; ++k) {
+                const int slot = k & 1;
+                if (!(ok = mbar_wait(smem_u32(&sm.item_full[slot]), (k >> 1) & 1, kWaitTimeoutNs, abort)))
+                    break;
+                const int item = sm.item[slot];
+                mbar_arrive(smem_u32(&sm.item_empty[slot]));
+                if (item < 0) break;
+                int bh, j;
+                dkdv_item(a, item, bh, j);
+                if (!(ok = mbar_wait(smem_u32(&sm.out_staged), k & 1, kWaitTimeoutNs, abort))) break;
+                for (int b = 0; b < Cfg::kBoxes; ++b)
+                    tma_store_3d(&tdk, smem_u32(sm.k) + b * kBBox, b * 64, j * 128, bh);
                 bulk_commit_group();
-                bulk_wait_group0();  // written out before the CTA leaves
-            } else {
-                bwd_timeout(a, abort);
+                for (int b = 0; b < Cfg::kBoxes; ++b)
+                    tma_store_3d(&tdv, smem_u32(sm.v) + b * kBBox, b * 64, j * 128, bh);
+                bulk_commit_group();
+                bulk_wait_group_read<1>();
+                mbar_arrive(smem_u32(&sm.k_free));
+                bulk_wait_group_read<0>();
+                mbar_arrive(smem_u32(&sm.v_free));
             }
+            if (!ok) bwd_timeout(a, abort);
+            bulk_wait_group0();  // written out before the CTA leaves
         }
     } else if (warp >= 4) {
         // ===================== compute =====================
         const int wg = (warp - 4) >> 2;  // query-column half of S^T / dP^T, and column half of dK/dV
         const int wq = warp & 3;
         const int row = wq * 32 + lane;   // TMEM lane: key row of S^T/dP^T/dK/dV
-        const int kglob = j * 128 + row;
         const uint32_t lane_addr = tbase + (static_cast<uint32_t>(wq * 32) << 16);
         const float sl2 = a.scale_log2;
-        const bool row_valid = kglob < N;
         bool ok = true;
-        for (int it = 0; it < niter; ++it) {
-            const int qs = it % Cfg::kQSlots, ds = it % Cfg::kDoSlots;
+        int g = 0;  // running query-tile count of this CTA, as in the MMA warp
+        for (int k = 0; ok; ++k) {
+          const int slot = k & 1;
+          if (!(ok = mbar_wait_warp(smem_u32(&sm.item_full[slot]), (k >> 1) & 1, kWaitTimeoutNs, abort)))
+              break;
+          const int item = sm.item[slot];
+          mbar_arrive(smem_u32(&sm.item_empty[slot]));
+          if (item < 0) break;
+          int bh, j;
+          dkdv_item(a, item, bh, j);
+          const int i_begin = a.causal ? j : 0;
+          const int niter = nq - i_begin;
+          const bool row_valid = j * 128 + row < N;
+          for (int it = 0; it < niter; ++it, ++g) {
+            const int qs = g % Cfg::kQSlots, ds = g % Cfg::kDoSlots;
             const int i = i_begin + it;
-            ok = mbar_wait_warp(smem_u32(&sm.s_full), it & 1, kWaitTimeoutNs, abort) &&
-                 mbar_wait_warp(smem_u32(&sm.q_full[qs]), (it / Cfg::kQSlots) & 1, kWaitTimeoutNs,
+            ok = mbar_wait_warp(smem_u32(&sm.s_full), g & 1, kWaitTimeoutNs, abort) &&
+                 mbar_wait_warp(smem_u32(&sm.q_full[qs]), (g / Cfg::kQSlots) & 1, kWaitTimeoutNs,
                                 abort);
             if (!ok) break;
             tc_fence_after();
@@ -452,8 +532,8 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                 }
             }
 
-            ok = mbar_wait_warp(smem_u32(&sm.dp_full), it & 1, kWaitTimeoutNs, abort) &&
-                 mbar_wait_warp(smem_u32(&sm.do_full[ds]), (it / Cfg::kDoSlots) & 1, kWaitTimeoutNs,
+            ok = mbar_wait_warp(smem_u32(&sm.dp_full), g & 1, kWaitTimeoutNs, abort) &&
+                 mbar_wait_warp(smem_u32(&sm.do_full[ds]), (g / Cfg::kDoSlots) & 1, kWaitTimeoutNs,
                                 abort);
             if (!ok) break;
             tc_fence_after();
@@ -483,21 +563,20 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(smem_u32(&sm.ds_ready));
-        }
-        if (!ok) {
-            if (lane == 0) bwd_timeout(a, abort);
-        } else {
-            ok = mbar_wait_warp(smem_u32(&sm.dkdv_done), 0, kWaitTimeoutNs, abort);
-            if (ok) {
-                tc_fence_after();
+          }
+          if (!ok) break;
+          if (!(ok = mbar_wait_warp(smem_u32(&sm.dkdv_done), k & 1, kWaitTimeoutNs, abort))) break;
+          tc_fence_after();
+          {
                 // this thread's row of columns [wg * d/2, (wg + 1) * d/2) of dV (into
-                // q[0]) and dK (into q[1]): 64-column boxes of 128-byte rows, 16-byte
-                // chunk c of row r at position c ^ (r % 8)
+                // the V buffer) and dK (into the K buffer), free since every MMA of the
+                // item is done: 64-column boxes of 128-byte rows, 16-byte chunk c of
+                // row r at position c ^ (r % 8)
                 constexpr int kHalf = HD / 2;
                 const int col0 = wg * kHalf;
                 const uint32_t row_off = static_cast<uint32_t>((col0 / 64) * kBBox + row * 128);
-                const uint32_t dv_row = smem_u32(sm.q[0]) + row_off;
-                const uint32_t dk_row = smem_u32(sm.q[1]) + row_off;
+                const uint32_t dv_row = smem_u32(sm.v) + row_off;
+                const uint32_t dk_row = smem_u32(sm.k) + row_off;
 #pragma unroll 1
                 for (int c = 0; c < kHalf; c += 32) {
                     uint32_t rv[32], rk[32];
@@ -521,12 +600,15 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                         st_shared_v4(dk_row + sw, pkk[4 * m], pkk[4 * m + 1], pkk[4 * m + 2], pkk[4 * m + 3]);
                     }
                 }
+                // the TMEM reads above come before the next item's first dV / dK, which
+                // can only be issued after these rows were stored out (barrier chain
+                // out_staged -> k_free -> kv_full)
+                tc_fence_before();
                 fence_proxy_async_smem();
                 mbar_arrive(smem_u32(&sm.out_staged));
-            } else if (lane == 0) {
-                bwd_timeout(a, abort);
-            }
+          }
         }
+        if (!ok && lane == 0) bwd_timeout(a, abort);
     }
 
     tc_fence_before();
@@ -546,7 +628,10 @@ cudaError_t launch_bwd_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, cons
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    const unsigned grid = static_cast<unsigned>(a.n_kblk) * static_cast<unsigned>(a.BH);
+    // persistent: one CTA per multiprocessor, work items handed out by a counter
+    if ((e = cudaMemsetAsync(a.work, 0, sizeof(unsigned), stream)) != cudaSuccess) return e;
+    const long long items = static_cast<long long>(a.n_kblk) * a.BH;
+    const unsigned grid = static_cast<unsigned>(items < a.sms ? items : a.sms);
     fa_bwd_dkdv_kernel<HD><<<grid, kBThreads, smem, stream>>>(tq, tk, tv, tdo, tdk, tdv, a);
     return cudaGetLastError();
 }

@@ -60,6 +60,8 @@ struct BwdArgs {
     // workspace, fp32 [BH, n_kblk * 128] (rows padded to whole 128-row tiles):
     float* delta;     // D = rowsum(dO * O); 0 in the padding
     float* nlse2;     // -lse * log2(e); -inf in the padding (P = 0 there)
+    unsigned* work;   // work-item counter of the dK/dV kernel (zeroed before each launch)
+    int sms;          // multiprocessors of the device (the dK/dV kernel's grid)
     int BH;
     int N;
     int n_kblk;       // 128-row key blocks per head (= 128-row query blocks)

@@ -22,10 +22,10 @@
 
 namespace {
 
-// 64 MiB: fa_bwd_workspace_size (8 bytes per row, rows padded to whole
-// 128-row tiles) must fit, i.e. up to 2^23 rows; larger sizes return
-// FA_ERR_WORKSPACE.
-constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;
+// 64 MiB and 256 bytes: fa_bwd_workspace_size (8 bytes per row, rows padded to
+// whole 128-row tiles, and a 256-byte work counter) must fit, i.e. up to 2^23
+// rows; larger sizes return FA_ERR_WORKSPACE.
+constexpr size_t kNoAllocScratchBytes = (size_t(64) << 20) + 256;
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];

@@ -59,7 +59,8 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
 
 /* Bytes of device workspace fa_bwd needs for these sizes: two fp32 row
  * statistics, D = rowsum(dO * O) and -lse * log2(e), each [B*H, N rounded up to
- * a multiple of 128] and rounded up to 256 bytes (d does not change it). */
+ * a multiple of 128] and rounded up to 256 bytes, then 256 bytes for the dK/dV
+ * kernel's work counter (d does not change it). */
 size_t fa_bwd_workspace_size(int B, int H, int N, int d);
 
 /* Backward pass.  Inputs q, k, v, o, lse (as written by fa_fwd) and dout
@@ -103,10 +104,10 @@ int fa_bwd_dq(const void* q, const void* k, const void* v, const float* lse,
  * footprint after start-up, or a plug-in whose host framework owns every
  * allocation.  (The pages have no counterpart: this is a packaging choice of
  * this library.)  Same arguments, results and errors as fa_bwd, minus the workspace: the
- * scratch (fa_bwd_workspace_size bytes) lives in one fixed 64 MiB array of
- * library device memory, so nothing is allocated.  Sizes whose workspace
- * exceeds 64 MiB (more than 2^23 rows B*H*N after rounding N up to a multiple
- * of 128) return FA_ERR_WORKSPACE before any launch.  The first call on a device looks up the array's device address with
+ * scratch (fa_bwd_workspace_size bytes) lives in one fixed array of 64 MiB +
+ * 256 bytes of library device memory, so nothing is allocated.  Sizes whose
+ * workspace exceeds it (more than 2^23 rows B*H*N after rounding N up to a
+ * multiple of 128) return FA_ERR_WORKSPACE before any launch.  The first call on a device looks up the array's device address with
  * that device current; make that first call before any stream capture.  Every
  * call on a device shares the array: calls whose work overlaps on the GPU
  * (other streams, unordered host threads) race on it. */

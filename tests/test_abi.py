@@ -48,7 +48,7 @@ def test_workspace_size(lib):
     B, H, N, d = 2, 3, 100, 64
     r256 = lambda x: (x + 255) // 256 * 256
     npad = B * H * ((N + 127) // 128) * 128
-    assert fa.fa_bwd_workspace_size(B, H, N, d) == 2 * r256(npad * 4)  # D, -lse * log2(e)
+    assert fa.fa_bwd_workspace_size(B, H, N, d) == 2 * r256(npad * 4) + 256  # D, -lse*log2(e), counter
     assert fa.fa_bwd_workspace_size(0, 1, 1, 64) == 0
 
 

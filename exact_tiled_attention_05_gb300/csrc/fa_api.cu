@@ -150,7 +150,7 @@ size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 size_t ws_half(int B, int H, int N) {
     return round256(static_cast<size_t>(B) * H * ((N + 127) / 128) * 128 * sizeof(float));
 }
-size_t ws_bytes(int B, int H, int N) { return 2 * ws_half(B, H, N) + 256; }  // + work counter
+size_t ws_bytes(int B, int H, int N) { return 2 * ws_half(B, H, N) + 256; }  // + work counters
 
 // FP8 workspace: segment offsets (each 256-byte aligned), in the order fa.h lists.
 struct Fp8Layout {

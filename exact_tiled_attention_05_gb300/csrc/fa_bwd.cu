@@ -165,13 +165,6 @@ __device__ __forceinline__ void dkdv_item(const BwdArgs& a, int t, int& bh, int&
 
 constexpr int kItemReaders = 2 + kBCompute;  // MMA thread, store thread, compute threads
 
-// Waits until at most N of this thread's committed bulk groups are still
-// reading their shared-memory source.
-template <int N>
-__device__ __forceinline__ void bulk_wait_group_read() {
-    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-
 __device__ __forceinline__ void bwd_timeout(const BwdArgs& a, volatile int* abort) {
     *abort = 1;
     atomicExch(a.status, kErrDeviceTimeout);
@@ -277,7 +270,7 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                 if (k >= 2 && !(ok = mbar_wait(smem_u32(&sm.item_empty[slot]), ((k - 2) >> 1) & 1,
                                                kWaitTimeoutNs, abort)))
                     break;
-                const unsigned t = atomicAdd(a.work, 1u);
+                const unsigned t = atomicAdd(a.work + kWorkDkdv, 1u);
                 const int item = t < static_cast<unsigned>(n_items) ? static_cast<int>(t) : -1;
                 sm.item[slot] = item;
                 mbar_arrive(smem_u32(&sm.item_full[slot]));
@@ -629,7 +622,7 @@ cudaError_t launch_bwd_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, cons
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     // persistent: one CTA per multiprocessor, work items handed out by a counter
-    if ((e = cudaMemsetAsync(a.work, 0, sizeof(unsigned), stream)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(a.work + kWorkDkdv, 0, sizeof(unsigned), stream)) != cudaSuccess) return e;
     const long long items = static_cast<long long>(a.n_kblk) * a.BH;
     const unsigned grid = static_cast<unsigned>(items < a.sms ? items : a.sms);
     fa_bwd_dkdv_kernel<HD><<<grid, kBThreads, smem, stream>>>(tq, tk, tv, tdo, tdk, tdv, a);

@@ -47,6 +47,10 @@ struct FwdArgs {
     int* status;      // device status word
 };
 
+// Counters of the persistent backward kernels inside BwdArgs::work, 128 bytes apart.
+constexpr int kWorkDkdv = 0;
+constexpr int kWorkDq = 32;
+
 struct BwdArgs {
     const void* q;    // bf16 [BH, N, d] (plain pointers for the row-wise stages)
     const void* k;
@@ -60,8 +64,9 @@ struct BwdArgs {
     // workspace, fp32 [BH, n_kblk * 128] (rows padded to whole 128-row tiles):
     float* delta;     // D = rowsum(dO * O); 0 in the padding
     float* nlse2;     // -lse * log2(e); -inf in the padding (P = 0 there)
-    unsigned* work;   // work-item counter of the dK/dV kernel (zeroed before each launch)
-    int sms;          // multiprocessors of the device (the dK/dV kernel's grid)
+    unsigned* work;   // 256-byte slot of work-item counters: [kWorkDkdv], [kWorkDq] (each
+                      // zeroed before its kernel's launch)
+    int sms;          // multiprocessors of the device (grid of the persistent kernels)
     int BH;
     int N;
     int n_kblk;       // 128-row key blocks per head (= 128-row query blocks)

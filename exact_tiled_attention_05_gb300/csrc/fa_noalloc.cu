@@ -23,7 +23,7 @@
 namespace {
 
 // 64 MiB and 256 bytes: fa_bwd_workspace_size (8 bytes per row, rows padded to
-// whole 128-row tiles, and a 256-byte work counter) must fit, i.e. up to 2^23
+// whole 128-row tiles, and 256 bytes of work counters) must fit, i.e. up to 2^23
 // rows; larger sizes return FA_ERR_WORKSPACE.
 constexpr size_t kNoAllocScratchBytes = (size_t(64) << 20) + 256;
 constexpr int kMaxDevices = 64;

@@ -59,8 +59,8 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
 
 /* Bytes of device workspace fa_bwd needs for these sizes: two fp32 row
  * statistics, D = rowsum(dO * O) and -lse * log2(e), each [B*H, N rounded up to
- * a multiple of 128] and rounded up to 256 bytes, then 256 bytes for the dK/dV
- * kernel's work counter (d does not change it). */
+ * a multiple of 128] and rounded up to 256 bytes, then 256 bytes for the work
+ * counters of the dK/dV and dQ kernels (d does not change it). */
 size_t fa_bwd_workspace_size(int B, int H, int N, int d);
 
 /* Backward pass.  Inputs q, k, v, o, lse (as written by fa_fwd) and dout
@@ -85,8 +85,9 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
  *       dQ = scale * dS K on chip; writes dq.
  * main and dq both read D from the workspace (written by prep) and nothing
  * else of each other, so they may run in either order or concurrently on
- * two streams once prep has finished.  Arguments mean the same as for
- * fa_bwd. */
+ * two streams once prep has finished.  Each takes its work items from its own
+ * counter in the workspace, so two calls of the same stage must not overlap
+ * on one workspace.  Arguments mean the same as for fa_bwd. */
 int fa_bwd_prep(const void* o, const void* dout, const float* lse, int B, int H, int N, int d,
                 void* workspace, size_t workspace_bytes, void* stream);
 int fa_bwd_main(const void* q, const void* k, const void* v, const float* lse,

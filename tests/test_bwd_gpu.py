@@ -96,6 +96,53 @@ def test_stage_entry_points_match_fa_bwd():
     assert torch.equal(dq1, dq2) and torch.equal(dk1, dk2) and torch.equal(dv1, dv2)
 
 
+@pytest.mark.parametrize("N,d", [(128, 128), (256, 128), (128, 64), (256, 64)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_many_short_items_per_cta(N, d, causal):
+    """400 heads of one or two 128-row tiles: the persistent dK/dV and dQ kernels
+    (one CTA per SM) each run several short work items back to back, so item
+    hand-over, the rings that run on across items and the per-item barriers are
+    exercised many times per CTA."""
+    B, H = 2, 200
+    scale = 1.0 / math.sqrt(d)
+    inp = small_inputs(B, H, N, d, seed=3000 + N + d + causal)
+    _, _, dq, dk, dv = gpu_fwd_bwd(inp, causal, scale)
+    heads = list(range(0, B * H, 7)) + [B * H - 1]
+    g = oracle.bwd(bits(inp["q"]), bits(inp["k"]), bits(inp["v"]), bits(inp["do"]), scale, causal,
+                   heads=heads)
+    for got, ref, name in ((dq, g[0], "dq"), (dk, g[1], "dk"), (dv, g[2], "dv")):
+        check_grad(to_np(got).reshape(B * H, N, d)[heads], ref, f"{name} N={N} d={d} causal={causal}")
+
+
+def test_main_and_dq_concurrently_on_two_streams():
+    """After prep, the dK/dV and dQ stages on two streams at once (each takes its
+    work items from its own counter in the workspace): bitwise equal to fa_bwd."""
+    B, H, N, d = 4, 16, 1024, 128
+    scale = 1.0 / math.sqrt(d)
+    inp = small_inputs(B, H, N, d, seed=11)
+    q, k, v, do = (inp[n].to(DEV) for n in ("q", "k", "v", "do"))
+    o, lse = fa.forward(q, k, v, causal=True)
+    dq1, dk1, dv1 = fa.backward(q, k, v, o, lse, do, causal=True)
+    ws = fa.alloc_workspace(B, H, N, d, DEV)
+    dq2, dk2, dv2 = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    main = torch.cuda.current_stream()
+    assert fa.fa_bwd_prep(o.data_ptr(), do.data_ptr(), lse.data_ptr(), B, H, N, d, ws.data_ptr(),
+                          ws.numel(), main.cuda_stream) == 0
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    s1.wait_stream(main)
+    s2.wait_stream(main)
+    assert fa.fa_bwd_main(q.data_ptr(), k.data_ptr(), v.data_ptr(), lse.data_ptr(), do.data_ptr(),
+                          dk2.data_ptr(), dv2.data_ptr(), B, H, N, d, scale, 1, ws.data_ptr(),
+                          ws.numel(), s1.cuda_stream) == 0
+    assert fa.fa_bwd_dq(q.data_ptr(), k.data_ptr(), v.data_ptr(), lse.data_ptr(), do.data_ptr(),
+                        dq2.data_ptr(), B, H, N, d, scale, 1, ws.data_ptr(), ws.numel(),
+                        s2.cuda_stream) == 0
+    main.wait_stream(s1)
+    main.wait_stream(s2)
+    fa.sync_status()
+    assert torch.equal(dq1, dq2) and torch.equal(dk1, dk2) and torch.equal(dv1, dv2)
+
+
 def test_guard_bands_and_workspace_reuse():
     B, H, N, d = 1, 3, 300, 64
     inp = small_inputs(B, H, N, d, seed=9)

@@ -268,6 +268,7 @@ def run_gpu(args, world, rank, local):
     lse = torch.empty(B, H, N, dtype=torch.float32, device=dev)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     ws = fa.alloc_workspace(B, H, N, d, dev)
+    fws = torch.empty(fa.fa_fwd_workspace_size(B, H, N, d), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     h = stream.cuda_stream
     scale = w.scale
@@ -280,7 +281,8 @@ def run_gpu(args, world, rank, local):
     def step(ev=None):
         if ev:
             ev[0].record(stream)
-        check(fa.fa_fwd(P(q), P(k), P(v), P(o), P(lse), B, H, N, d, scale, 1, h), "fa_fwd")
+        check(fa.fa_fwd(P(q), P(k), P(v), P(o), P(lse), B, H, N, d, scale, 1, P(fws), fws.numel(), h),
+              "fa_fwd")
         if ev:
             ev[1].record(stream)
         check(fa.fa_bwd_prep(P(o), P(do), P(lse), B, H, N, d, P(ws), ws.numel(), h), "fa_bwd_prep")
@@ -392,7 +394,7 @@ def run_gpu(args, world, rank, local):
                 s_cmp.wait_event(out_done[b])  # step k-2's results have left the device
             x, y = dev_in[b], dev_out[b]
             fa.forward(x["q"], x["k"], x["v"], scale=scale, causal=True, out=y["o"], lse=y["lse"],
-                       stream=s_cmp)
+                       workspace=fws, stream=s_cmp)
             fa.backward(x["q"], x["k"], x["v"], y["o"], y["lse"], x["do"], scale=scale, causal=True,
                         dq=y["dq"], dk=y["dk"], dv=y["dv"], workspace=ws, stream=s_cmp)
             cmp_done[b].record(s_cmp)
@@ -430,13 +432,13 @@ def run_gpu(args, world, rank, local):
     go = torch.empty_like(gin["q"])
     gl = torch.empty(wg.B, wg.H, wg.N, dtype=torch.float32, device=dev)
     for _ in range(3):
-        fa.forward(gin["q"], gin["k"], gin["v"], causal=True, out=go, lse=gl)
+        fa.forward(gin["q"], gin["k"], gin["v"], causal=True, out=go, lse=gl, workspace=fws)
     reps = 50
     fe = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
     torch.cuda.synchronize(dev)
     for a_, b_ in fe:
         a_.record(stream)
-        fa.forward(gin["q"], gin["k"], gin["v"], causal=True, out=go, lse=gl)
+        fa.forward(gin["q"], gin["k"], gin["v"], causal=True, out=go, lse=gl, workspace=fws)
         b_.record(stream)
     torch.cuda.synchronize(dev)
     check(fa.fa_sync_status(h), "forward gate")
@@ -459,13 +461,13 @@ def run_gpu(args, world, rank, local):
     lo = torch.empty_like(lin["q"])
     ll = torch.empty(wl32.B, wl32.H, wl32.N, dtype=torch.float32, device=dev)
     for _ in range(3):
-        fa.forward(lin["q"], lin["k"], lin["v"], causal=True, out=lo, lse=ll)
+        fa.forward(lin["q"], lin["k"], lin["v"], causal=True, out=lo, lse=ll, workspace=fws)
     lreps = 10
     le = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(lreps)]
     torch.cuda.synchronize(dev)
     for a_, b_ in le:
         a_.record(stream)
-        fa.forward(lin["q"], lin["k"], lin["v"], causal=True, out=lo, lse=ll)
+        fa.forward(lin["q"], lin["k"], lin["v"], causal=True, out=lo, lse=ll, workspace=fws)
         b_.record(stream)
     torch.cuda.synchronize(dev)
     check(fa.fa_sync_status(h), "forward 32k")

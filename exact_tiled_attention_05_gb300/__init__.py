@@ -24,7 +24,7 @@ FA_ERR_CUDA = 5
 FA_ERR_DEVICE_TIMEOUT = 6
 
 EXPORTED = (
-    "fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_bwd_prep", "fa_bwd_main",
+    "fa_fwd", "fa_fwd_workspace_size", "fa_bwd", "fa_bwd_workspace_size", "fa_bwd_prep", "fa_bwd_main",
     "fa_bwd_dq", "fa_bwd_noalloc", "fa_fp8_workspace_size", "fa_fp8_quantize", "fa_fwd_fp8",
     "fa_sync_status", "fa_status_string", "fa_version",
 )
@@ -53,7 +53,8 @@ def load_library(path: str = LIB_PATH):
     lib = ctypes.CDLL(path)
     P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     sig = {
-        "fa_fwd": ([P, P, P, P, P, I, I, I, I, F, I, P], I),
+        "fa_fwd": ([P, P, P, P, P, I, I, I, I, F, I, P, Z, P], I),
+        "fa_fwd_workspace_size": ([I, I, I, I], Z),
         "fa_bwd_workspace_size": ([I, I, I, I], Z),
         "fa_bwd": ([P, P, P, P, P, P, P, P, P, I, I, I, I, F, I, P, Z, P], I),
         "fa_bwd_prep": ([P, P, P, I, I, I, I, P, Z, P], I),
@@ -79,8 +80,12 @@ def load_library(path: str = LIB_PATH):
 # one-to-one wrappers of the C ABI (pointers as Python ints)
 # ---------------------------------------------------------------------------
 
-def fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, stream):
-    return load_library().fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, stream)
+def fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, ws, ws_bytes, stream):
+    return load_library().fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, ws, ws_bytes, stream)
+
+
+def fa_fwd_workspace_size(B, H, N, d):
+    return load_library().fa_fwd_workspace_size(B, H, N, d)
 
 
 def fa_bwd_workspace_size(B, H, N, d):
@@ -166,6 +171,13 @@ def _stream_handle(stream=None) -> int:
     return int(s.cuda_stream)
 
 
+def _keep_for_stream(t, stream):
+    """A scratch tensor allocated here and used by work enqueued on `stream`:
+    keep the caching allocator from reusing its memory until that work is done."""
+    if stream is not None:
+        t.record_stream(stream)
+
+
 def _check_qkv(*ts):
     torch = _torch()
     ref = ts[0]
@@ -179,9 +191,12 @@ def _check_qkv(*ts):
     return tuple(ref.shape)
 
 
-def forward(q, k, v, scale=None, causal=False, out=None, lse=None, stream=None):
+def forward(q, k, v, scale=None, causal=False, out=None, lse=None, workspace=None, stream=None):
     """O, lse = attention(q, k, v).  q, k, v: bf16 [B, H, N, d] on the GPU.
-    Returns (o bf16 [B,H,N,d], lse fp32 [B,H,N])."""
+    Returns (o bf16 [B,H,N,d], lse fp32 [B,H,N]).  `workspace` (uint8 CUDA
+    tensor of fa_fwd_workspace_size bytes) holds the kernel's work counter; one
+    is allocated when none is given.  workspace=False runs without one (one CTA
+    per work item)."""
     torch = _torch()
     B, H, N, d = _check_qkv(q, k, v)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
@@ -192,8 +207,13 @@ def forward(q, k, v, scale=None, causal=False, out=None, lse=None, stream=None):
     _check_qkv(q, out)
     if lse.dtype != torch.float32 or not lse.is_contiguous() or lse.shape != (B, H, N):
         raise ValueError("lse must be contiguous fp32 [B, H, N]")
+    if workspace is None:
+        workspace = torch.empty(int(fa_fwd_workspace_size(B, H, N, d)), dtype=torch.uint8,
+                                device=q.device)
+        _keep_for_stream(workspace, stream)
+    ws_ptr, ws_bytes = (0, 0) if workspace is False else (workspace.data_ptr(), workspace.numel())
     rc = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
-                B, H, N, d, scale, int(bool(causal)), _stream_handle(stream))
+                B, H, N, d, scale, int(bool(causal)), ws_ptr, ws_bytes, _stream_handle(stream))
     _check(rc, "fa_fwd")
     return out, lse
 
@@ -221,6 +241,7 @@ def backward(q, k, v, o, lse, dout, scale=None, causal=False, dq=None, dk=None, 
         raise ValueError("lse must be contiguous fp32 [B, H, N]")
     if workspace is None:
         workspace = alloc_workspace(B, H, N, d, q.device)
+        _keep_for_stream(workspace, stream)
     rc = fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
                 dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
                 B, H, N, d, scale, int(bool(causal)), workspace.data_ptr(), workspace.numel(),

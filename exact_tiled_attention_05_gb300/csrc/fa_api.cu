@@ -263,7 +263,7 @@ using namespace fa;
 
 extern "C" {
 
-int fa_version(void) { return 300; }
+int fa_version(void) { return 400; }
 
 const char* fa_status_string(int status) {
     switch (status) {
@@ -278,11 +278,19 @@ const char* fa_status_string(int status) {
     }
 }
 
+size_t fa_fwd_workspace_size(int B, int H, int N, int d) {
+    if (B < 1 || H < 1 || N < 1 || d < 1) return 0;
+    return 256;
+}
+
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
-           int d, float scale, int causal, void* stream) {
+           int d, float scale, int causal, void* workspace, size_t workspace_bytes, void* stream) {
     if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
     int rc = check_shape(B, H, N, d, scale, causal);
     if (rc) return rc;
+    if (workspace && (((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) ||
+                      workspace_bytes < fa_fwd_workspace_size(B, H, N, d)))
+        return FA_ERR_WORKSPACE;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
         (reinterpret_cast<uintptr_t>(lse) & 3u))
         return FA_ERR_MISALIGNED;
@@ -303,6 +311,8 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
     a.group = clampi(floor_pow2(clampi((2 * current_sms()) / a.n_qblk, 1, 1 << 20)), 1, BH);
     a.causal = causal;
     a.scale_log2 = scale * 1.4426950408889634f;
+    a.work = static_cast<unsigned*>(workspace);
+    a.sms = current_sms();
     return map_cuda(launch_fwd(d, tq, tk, tv, to, a, static_cast<cudaStream_t>(stream)));
 }
 

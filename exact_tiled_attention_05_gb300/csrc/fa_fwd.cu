@@ -1,11 +1,18 @@
 // fa_fwd.cu -- fused exact-attention forward pass for sm_103a.
 //
-// One CTA owns 256 query rows of one (batch, head): two 128-row Q tiles that
-// share every K/V tile it streams ("FlashAttention 1–4" §"FlashAttention-2":
-// a thread block per query block, K/V streamed in the inner loop; two Q tiles
-// per CTA as in §"FlashAttention-4").  Roles, by warp:
-//   warp 0       TMA producer: Q tiles once, then K_j, V_j into a ring of
-//                shared-memory stages guarded by full/empty mbarriers.
+// A work item is 256 query rows of one (batch, head): two 128-row Q tiles that
+// share every K/V tile streamed for them ("FlashAttention 1–4"
+// §"FlashAttention-2": a thread block per query block, K/V streamed in the
+// inner loop; two Q tiles per CTA as in §"FlashAttention-4").  With a work
+// counter the kernel is persistent: one CTA per SM takes items until none are
+// left, and the K/V ring, TMEM buffers and barrier phases run on across items,
+// so the next item's Q, K_0 and first S are under way while the softmax warps
+// still write out the previous item's O.  Without one, each CTA takes the item
+// of its block index.  Roles, by warp:
+//   warp 0       TMA producer and work fetch: Q tiles once per item (each
+//                buffer once the previous item's last S has read it), K_j, V_j
+//                into a ring of shared-memory stages guarded by full/empty
+//                mbarriers.
 //   warp 1       MMA issuer (and TMEM allocation): S_t = Q_t K_j^T and
 //                O_t += P_t V_j on the tcgen05 tensor cores, accumulators in
 //                tensor memory (TMEM).
@@ -16,8 +23,9 @@
 //                the causal/tail mask, runs the online-softmax update and writes
 //                P (bf16) back into TMEM over S in two parts (keys 0-63, then
 //                64-127), each handed to the MMA warp as soon as it is stored.
-//                At the end it normalises O into the tile's Q buffer, which the
-//                producer warp writes out with TMA, and writes lse.
+//                At the end of an item it normalises O into a staging buffer
+//                (one tile at a time) and writes lse.
+//   warp 18      O stores: TMA tile stores of the staged tiles.
 //
 // Online softmax ("07 GPU、资源估算与 FlashAttention" §7.8; "CS336 Lecture 5
 // notes" §11.3-§11.4): per row a running max m (log2 units of the scaled
@@ -38,8 +46,9 @@ using namespace ptx;
 
 constexpr int kBM = 128;        // query rows per Q tile
 constexpr int kBN = 128;        // keys per K/V tile
-constexpr int kThreads = 576;   // 18 warps: TMA, MMA (+TMEM allocation), 2 tiles x 8 softmax
+constexpr int kThreads = 608;   // 19 warps: TMA, MMA (+TMEM allocation), 2 tiles x 8 softmax, stores
 constexpr int kFirstSoftmaxWarp = 2;
+constexpr int kStoreWarp = 18;
 constexpr int kSoftmaxPerTile = 256;  // threads per Q tile: a quad per pair of rows
 constexpr int kBoxBytes = 128 * 64 * 2;  // one TMA box: 128 rows x 64 bf16
 // Conditional rescaling ("FlashAttention 1–4" §"FlashAttention-4"): the
@@ -121,6 +130,7 @@ __device__ __forceinline__ void tmem_st_16x128b_x8(uint32_t taddr, const uint32_
         : "memory");
 }
 
+
 template <int HD>
 struct FwdCfg {
     static constexpr int kTileBytes = kBN * HD * 2;
@@ -135,13 +145,18 @@ template <int HD>
 struct alignas(1024) FwdSmem {
     uint8_t q[2][FwdCfg<HD>::kTileBytes];
     uint8_t kv[FwdCfg<HD>::kStages][FwdCfg<HD>::kTileBytes];
-    uint64_t q_full;
+    uint8_t o[FwdCfg<HD>::kTileBytes];  // one normalised O tile waiting for its TMA store
+    int item[2];                           // work items published by the producer (-1: none left)
+    uint64_t item_full[2], item_empty[2];  // per queue slot: written / read by every role
+    uint64_t q_full[2];   // per Q tile: landed
+    uint64_t q_free[2];   // per Q tile: the item's last S has read it
     uint64_t kv_full[FwdCfg<HD>::kStages];
     uint64_t kv_empty[FwdCfg<HD>::kStages];
     uint64_t s_full[2];
     uint64_t p_full[2][kPParts];  // [tile][part of P]
     uint64_t o_done[2];
-    uint64_t out_staged[2];  // per tile: every softmax thread has staged its O rows
+    uint64_t out_staged;  // the softmax threads of one tile have staged its O rows
+    uint64_t o_free;      // the store thread has read the staged tile out
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
@@ -150,9 +165,57 @@ struct alignas(1024) FwdSmem {
 static_assert(sizeof(FwdSmem<128>) + 1024 <= 232448, "forward d=128 shared memory exceeds 227 KB");
 static_assert(sizeof(FwdSmem<64>) + 1024 <= 232448, "forward d=64 shared memory exceeds 227 KB");
 
+constexpr int kItemReaders = 2 + 2 * kSoftmaxPerTile;  // MMA thread, store thread, softmax threads
+
 __device__ __forceinline__ void record_timeout(FwdArgs const& a, volatile int* abort) {
     *abort = 1;
     atomicExch(a.status, kErrDeviceTimeout);
+}
+
+// Work item t (fetch order) -> (head, 256-row query block) and the key tiles
+// of its two Q tiles.  Causal: heads in groups of a.group; inside a group the
+// heaviest query blocks (the longest key ranges) come first, so taking items
+// in order approximates longest-processing-time-first while the K/V of the
+// heads in flight stay in L2.
+struct FwdItem {
+    int bh, q0[2], nkv[2], nmax;
+};
+
+__device__ __forceinline__ FwdItem fwd_item(const FwdArgs& a, int t) {
+    FwdItem it;
+    int qb;
+    if (a.causal) {
+        const int grp = t / (a.group * a.n_qblk);
+        const int first = grp * a.group;
+        const int gc = min(a.group, a.BH - first);
+        const int r = t - grp * a.group * a.n_qblk;
+        qb = a.n_qblk - 1 - r / gc;
+        it.bh = first + r % gc;
+    } else {
+        it.bh = t / a.n_qblk;
+        qb = t % a.n_qblk;
+    }
+    const int n_kv_all = (a.N + kBN - 1) / kBN;
+    for (int u = 0; u < 2; ++u) {
+        it.q0[u] = qb * 2 * kBM + u * kBM;
+        if (it.q0[u] >= a.N) {
+            it.nkv[u] = 0;  // tile beyond the sequence: inactive
+        } else if (a.causal) {
+            it.nkv[u] = (min(it.q0[u] + kBM, a.N) - 1) / kBN + 1;
+        } else {
+            it.nkv[u] = n_kv_all;
+        }
+    }
+    it.nmax = max(it.nkv[0], it.nkv[1]);
+    return it;
+}
+
+// Next work item of this CTA: from the counter when the launch is persistent,
+// else the CTA's own block index once.
+__device__ __forceinline__ int fwd_fetch(const FwdArgs& a, int k, int n_items) {
+    const unsigned t = a.work ? atomicAdd(a.work, 1u)
+                              : (k == 0 ? blockIdx.x : static_cast<unsigned>(n_items));
+    return t < static_cast<unsigned>(n_items) ? static_cast<int>(t) : -1;
 }
 
 template <int HD>
@@ -169,55 +232,28 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int N = args.N;
-    const int BH = args.BH;
-
-    // ---- work unit: (head, 256-row query block) ----
-    // Causal: heads are taken in groups of args.group; inside a group the
-    // heaviest query blocks (the longest key ranges) launch first, so the
-    // block scheduler approximates longest-processing-time-first while the
-    // K/V of the heads in flight stay in L2.
-    int bh, qb;
-    if (args.causal) {
-        const int b = static_cast<int>(blockIdx.x);
-        const int grp = b / (args.group * args.n_qblk);
-        const int first = grp * args.group;
-        const int gc = min(args.group, BH - first);
-        const int r = b - grp * args.group * args.n_qblk;
-        qb = args.n_qblk - 1 - r / gc;
-        bh = first + r % gc;
-    } else {
-        bh = static_cast<int>(blockIdx.x) / args.n_qblk;
-        qb = static_cast<int>(blockIdx.x) % args.n_qblk;
-    }
-    const int n_kv_all = (N + kBN - 1) / kBN;
-    int q0[2], nkv[2];
-    for (int t = 0; t < 2; ++t) {
-        q0[t] = qb * 2 * kBM + t * kBM;
-        if (q0[t] >= N) {
-            nkv[t] = 0;  // tile beyond the sequence: inactive
-        } else if (args.causal) {
-            const int last_q = min(q0[t] + kBM, N) - 1;
-            nkv[t] = last_q / kBN + 1;
-        } else {
-            nkv[t] = n_kv_all;
-        }
-    }
-    const int nmax = max(nkv[0], nkv[1]);
+    const int n_items = args.BH * args.n_qblk;
 
     if (threadIdx.x == 0) {
         sm.abort = 0;
-        mbar_init(smem_u32(&sm.q_full), 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(smem_u32(&sm.item_full[s]), 1);
+            mbar_init(smem_u32(&sm.item_empty[s]), kItemReaders);
+        }
         for (int s = 0; s < Cfg::kStages; ++s) {
             mbar_init(smem_u32(&sm.kv_full[s]), 1);
             mbar_init(smem_u32(&sm.kv_empty[s]), 1);
         }
         for (int t = 0; t < 2; ++t) {
+            mbar_init(smem_u32(&sm.q_full[t]), 1);
+            mbar_init(smem_u32(&sm.q_free[t]), 1);
             mbar_init(smem_u32(&sm.s_full[t]), 1);
             for (int part = 0; part < kPParts; ++part)
                 mbar_init(smem_u32(&sm.p_full[t][part]), kSoftmaxPerTile);
             mbar_init(smem_u32(&sm.o_done[t]), 1);
-            mbar_init(smem_u32(&sm.out_staged[t]), kSoftmaxPerTile);
         }
+        mbar_init(smem_u32(&sm.out_staged), kSoftmaxPerTile);
+        mbar_init(smem_u32(&sm.o_free), 1);
         mbar_init(smem_u32(&sm.drain), 1);
         fence_mbar_init();
     }
@@ -231,58 +267,69 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
     const uint32_t tbase = sm.tmem_base;
 
     if (warp == 0) {
-        // ===================== TMA producer =====================
-        if (elect_one()) {
+        // ===================== TMA producer and work fetch =====================
+        // Per item: fetch it and publish it to the other roles; Q_0, K_0, Q_1 (each
+        // Q buffer once the previous item's last S on it has completed), then the
+        // rest of the item's K_j, V_j into the ring, whose positions run on across
+        // items.
+        if (lane == 0) {
             tma_prefetch_desc(&tq);
             tma_prefetch_desc(&tk);
             tma_prefetch_desc(&tv);
-            const uint32_t qbar = smem_u32(&sm.q_full);
-            const int nact = (nkv[0] > 0) + (nkv[1] > 0);
-            mbar_arrive_expect_tx(qbar, nact * Cfg::kTileBytes);
-            for (int t = 0; t < 2; ++t) {
-                if (nkv[t] == 0) continue;
-                for (int b = 0; b < Cfg::kBoxes; ++b)
-                    tma_load_3d(smem_u32(sm.q[t] + b * kBoxBytes), &tq, qbar, b * 64, q0[t], bh);
-            }
-            int issued = 0;
             bool ok = true;
-            const int n_loads = FA_FAULT_INJECT ? 0 : 2 * nmax;
-            for (int idx = 0; idx < n_loads; ++idx) {
-                const int slot = idx % Cfg::kStages;
-                const uint32_t ph = (idx / Cfg::kStages) & 1;
-                if (!mbar_wait(smem_u32(&sm.kv_empty[slot]), ph ^ 1, kWaitTimeoutNs, abort)) {
-                    record_timeout(args, abort);
-                    ok = false;
+            int issued = 0;        // ring positions loaded
+            int nq[2] = {0, 0};    // Q loads per tile
+            for (int k = 0; ok; ++k) {
+                const int slot = k & 1;
+                if (k >= 2 && !(ok = mbar_wait(smem_u32(&sm.item_empty[slot]), ((k - 2) >> 1) & 1,
+                                               kWaitTimeoutNs, abort)))
                     break;
-                }
-                const uint32_t fbar = smem_u32(&sm.kv_full[slot]);
-                mbar_arrive_expect_tx(fbar, Cfg::kTileBytes);
-                const CUtensorMap* map = (idx & 1) ? &tv : &tk;
-                const int row = (idx >> 1) * kBN;
-                for (int b = 0; b < Cfg::kBoxes; ++b)
-                    tma_load_3d(smem_u32(sm.kv[slot] + b * kBoxBytes), map, fbar, b * 64, row, bh);
-                ++issued;
+                const int item = fwd_fetch(args, k, n_items);
+                sm.item[slot] = item;
+                mbar_arrive(smem_u32(&sm.item_full[slot]));
+                if (item < 0) break;
+                const FwdItem it = fwd_item(args, item);
+                auto load_q = [&](int u) -> bool {
+                    if (it.nkv[u] == 0) return true;
+                    if (nq[u] > 0 && !mbar_wait(smem_u32(&sm.q_free[u]), (nq[u] - 1) & 1,
+                                                kWaitTimeoutNs, abort))
+                        return false;
+                    const uint32_t qbar = smem_u32(&sm.q_full[u]);
+                    mbar_arrive_expect_tx(qbar, Cfg::kTileBytes);
+                    for (int b = 0; b < Cfg::kBoxes; ++b)
+                        tma_load_3d(smem_u32(sm.q[u] + b * kBoxBytes), &tq, qbar, b * 64, it.q0[u], it.bh);
+                    ++nq[u];
+                    return true;
+                };
+                // load idx of the item: K_{idx/2} for even idx, V_{idx/2} for odd
+                auto load_kv = [&](int idx) -> bool {
+                    const int s = issued % Cfg::kStages;
+                    if (!mbar_wait(smem_u32(&sm.kv_empty[s]), ((issued / Cfg::kStages) & 1) ^ 1,
+                                   kWaitTimeoutNs, abort))
+                        return false;
+                    const uint32_t fbar = smem_u32(&sm.kv_full[s]);
+                    mbar_arrive_expect_tx(fbar, Cfg::kTileBytes);
+                    const CUtensorMap* map = (idx & 1) ? &tv : &tk;
+                    for (int b = 0; b < Cfg::kBoxes; ++b)
+                        tma_load_3d(smem_u32(sm.kv[s] + b * kBoxBytes), map, fbar, b * 64,
+                                    (idx >> 1) * kBN, it.bh);
+                    ++issued;
+                    return true;
+                };
+                const int n_loads = FA_FAULT_INJECT ? 0 : 2 * it.nmax;
+                if (!(ok = load_q(0))) break;
+                if (n_loads > 0 && !(ok = load_kv(0))) break;
+                if (!(ok = load_q(1))) break;
+                for (int idx = 1; ok && idx < n_loads; ++idx) ok = load_kv(idx);
             }
+            if (!ok) record_timeout(args, abort);
             // Let every copy that was issued land before the CTA can exit.
-            for (int slot = 0; slot < Cfg::kStages && slot < issued; ++slot) {
-                const int last = slot + Cfg::kStages * ((issued - 1 - slot) / Cfg::kStages);
-                mbar_wait_drain(smem_u32(&sm.kv_full[slot]), (last / Cfg::kStages) & 1,
-                                kWaitTimeoutNs);
+            for (int s = 0; s < Cfg::kStages && s < issued; ++s) {
+                const int last = s + Cfg::kStages * ((issued - 1 - s) / Cfg::kStages);
+                mbar_wait_drain(smem_u32(&sm.kv_full[s]), (last / Cfg::kStages) & 1, kWaitTimeoutNs);
             }
-            mbar_wait_drain(qbar, 0, kWaitTimeoutNs);
-            // O of each tile, staged by the softmax warps over the tile's Q buffer
-            tma_prefetch_desc(&to);
-            for (int t = 0; ok && t < 2; ++t) {
-                if (nkv[t] == 0) continue;
-                if (!(ok = mbar_wait(smem_u32(&sm.out_staged[t]), 0, kWaitTimeoutNs, abort))) {
-                    record_timeout(args, abort);
-                    break;
-                }
-                for (int b = 0; b < Cfg::kBoxes; ++b)
-                    tma_store_3d(&to, smem_u32(sm.q[t]) + b * kBoxBytes, b * 64, q0[t], bh);
-            }
-            bulk_commit_group();
-            bulk_wait_group0();  // written out before the CTA leaves
+            for (int u = 0; u < 2; ++u)
+                if (nq[u] > 0) mbar_wait_drain(smem_u32(&sm.q_full[u]), (nq[u] - 1) & 1, kWaitTimeoutNs);
         }
     } else if (warp == 1) {
         // ===================== MMA issuer =====================
@@ -290,12 +337,11 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
             constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, 0, 0);
             constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, HD, 0, 1);
             const uint32_t q_addr[2] = {smem_u32(sm.q[0]), smem_u32(sm.q[1])};
-            bool ok = mbar_wait(smem_u32(&sm.q_full), 0, kWaitTimeoutNs, abort);
-            auto wait_kv = [&](int idx) -> bool {
-                return mbar_wait(smem_u32(&sm.kv_full[idx % Cfg::kStages]),
-                                 (idx / Cfg::kStages) & 1, kWaitTimeoutNs, abort);
+            auto wait_kv = [&](int pos) -> bool {
+                return mbar_wait(smem_u32(&sm.kv_full[pos % Cfg::kStages]),
+                                 (pos / Cfg::kStages) & 1, kWaitTimeoutNs, abort);
             };
-            auto kv_addr = [&](int idx) -> uint32_t { return smem_u32(sm.kv[idx % Cfg::kStages]); };
+            auto kv_addr = [&](int pos) -> uint32_t { return smem_u32(sm.kv[pos % Cfg::kStages]); };
             // S_t = Q_t K^T : K-major A and B, HD/16 k-steps of 16.
             auto issue_s = [&](int t, uint32_t k_addr) {
 #pragma unroll
@@ -316,54 +362,103 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                             (acc || part > 0 || i > 0) ? 1u : 0u);
                 }
             };
-            if (ok && nmax > 0) {
-                ok = wait_kv(0);
-                if (ok) {
-                    tc_fence_after();
-                    for (int t = 0; t < 2; ++t) {
-                        if (nkv[t] == 0) continue;
-                        issue_s(t, kv_addr(0));
-                        umma_commit(smem_u32(&sm.s_full[t]));
-                    }
-                    umma_commit(smem_u32(&sm.kv_empty[0]));
-                }
-            }
-            for (int j = 0; ok && j < nmax; ++j) {
-                const int iv = 2 * j + 1, ik = 2 * j + 2;
-                if (!(ok = wait_kv(iv))) break;
-                tc_fence_after();
-                bool k_ready = false;
+            bool ok = true;
+            int pos = 0;              // ring position of the item's K_0
+            int cnt[2] = {0, 0};      // S_t issued before the item (phases of s_full, p_full, o_done)
+            int nq[2] = {0, 0};       // Q_t loads consumed
+            for (int k = 0; ok; ++k) {
+                const int slot = k & 1;
+                if (!(ok = mbar_wait(smem_u32(&sm.item_full[slot]), (k >> 1) & 1, kWaitTimeoutNs, abort)))
+                    break;
+                const int item = sm.item[slot];
+                mbar_arrive(smem_u32(&sm.item_empty[slot]));
+                if (item < 0) break;
+                const FwdItem it = fwd_item(args, item);
+                // S_t(0) over P_t of the previous item, whose P V was issued before it
+                // (the tensor pipe executes one thread's MMAs in order)
+                if (!(ok = wait_kv(pos))) break;
                 for (int t = 0; t < 2 && ok; ++t) {
-                    if (j < nkv[t]) {
-                        for (int part = 0; part < kPParts && ok; ++part) {
-                            if (!(ok = mbar_wait(smem_u32(&sm.p_full[t][part]), j & 1, kWaitTimeoutNs,
-                                                 abort)))
-                                break;
-                            tc_fence_after();
-                            issue_pv(t, kv_addr(iv), part, j > 0);
-                        }
-                        if (!ok) break;
-                        umma_commit(smem_u32(&sm.o_done[t]));
-                    }
-                    if (t == 1) umma_commit(smem_u32(&sm.kv_empty[iv % Cfg::kStages]));
-                    if (j + 1 < nkv[t]) {
-                        if (!k_ready) {
-                            if (!(ok = wait_kv(ik))) break;
-                            tc_fence_after();
-                            k_ready = true;
-                        }
-                        // S_t(j+1) overwrites P_t(j) only after PV_t(j) was issued;
-                        // the tensor pipe executes one thread's MMAs in order.
-                        issue_s(t, kv_addr(ik));
-                        umma_commit(smem_u32(&sm.s_full[t]));
-                    }
+                    if (it.nkv[t] == 0) continue;
+                    if (!(ok = mbar_wait(smem_u32(&sm.q_full[t]), nq[t] & 1, kWaitTimeoutNs, abort))) break;
+                    ++nq[t];
+                    tc_fence_after();
+                    issue_s(t, kv_addr(pos));
+                    umma_commit(smem_u32(&sm.s_full[t]));
+                    if (it.nkv[t] == 1) umma_commit(smem_u32(&sm.q_free[t]));  // the item's last S_t
                 }
-                if (ok && k_ready) umma_commit(smem_u32(&sm.kv_empty[ik % Cfg::kStages]));
+                if (!ok) break;
+                umma_commit(smem_u32(&sm.kv_empty[pos % Cfg::kStages]));
+                for (int j = 0; ok && j < it.nmax; ++j) {
+                    const int iv = pos + 2 * j + 1, ik = pos + 2 * j + 2;
+                    if (!(ok = wait_kv(iv))) break;
+                    tc_fence_after();
+                    bool k_ready = false;
+                    for (int t = 0; t < 2 && ok; ++t) {
+                        if (j < it.nkv[t]) {
+                            for (int part = 0; part < kPParts && ok; ++part) {
+                                if (!(ok = mbar_wait(smem_u32(&sm.p_full[t][part]), (cnt[t] + j) & 1,
+                                                     kWaitTimeoutNs, abort)))
+                                    break;
+                                tc_fence_after();
+                                issue_pv(t, kv_addr(iv), part, j > 0);
+                            }
+                            if (!ok) break;
+                            umma_commit(smem_u32(&sm.o_done[t]));
+                        }
+                        if (t == 1) umma_commit(smem_u32(&sm.kv_empty[iv % Cfg::kStages]));
+                        if (j + 1 < it.nkv[t]) {
+                            if (!k_ready) {
+                                if (!(ok = wait_kv(ik))) break;
+                                tc_fence_after();
+                                k_ready = true;
+                            }
+                            // S_t(j+1) overwrites P_t(j) only after PV_t(j) was issued.
+                            issue_s(t, kv_addr(ik));
+                            umma_commit(smem_u32(&sm.s_full[t]));
+                            if (j + 2 == it.nkv[t]) umma_commit(smem_u32(&sm.q_free[t]));  // last S_t
+                        }
+                    }
+                    if (ok && k_ready) umma_commit(smem_u32(&sm.kv_empty[ik % Cfg::kStages]));
+                }
+                pos += 2 * it.nmax;
+                cnt[0] += it.nkv[0];
+                cnt[1] += it.nkv[1];
             }
             if (!ok) record_timeout(args, abort);
             // Every MMA (and every commit before it) completes before the CTA leaves.
             umma_commit(smem_u32(&sm.drain));
             mbar_wait_drain(smem_u32(&sm.drain), 0, kWaitTimeoutNs);
+        }
+    } else if (warp == kStoreWarp) {
+        // ===================== O stores =====================
+        // Per item and active Q tile (tile 0 first): the normalised tile staged in
+        // sm.o goes out with TMA tile stores; the buffer is handed back to the
+        // softmax warps as soon as the copy has read it.
+        if (elect_one()) {
+            tma_prefetch_desc(&to);
+            bool ok = true;
+            int u = 0;  // staged tiles so far
+            for (int k = 0; ok; ++k) {
+                const int slot = k & 1;
+                if (!(ok = mbar_wait(smem_u32(&sm.item_full[slot]), (k >> 1) & 1, kWaitTimeoutNs, abort)))
+                    break;
+                const int item = sm.item[slot];
+                mbar_arrive(smem_u32(&sm.item_empty[slot]));
+                if (item < 0) break;
+                const FwdItem it = fwd_item(args, item);
+                for (int t = 0; t < 2 && ok; ++t) {
+                    if (it.nkv[t] == 0) continue;
+                    if (!(ok = mbar_wait(smem_u32(&sm.out_staged), u & 1, kWaitTimeoutNs, abort))) break;
+                    for (int b = 0; b < Cfg::kBoxes; ++b)
+                        tma_store_3d(&to, smem_u32(sm.o) + b * kBoxBytes, b * 64, it.q0[t], it.bh);
+                    bulk_commit_group();
+                    bulk_wait_group_read<0>();
+                    mbar_arrive(smem_u32(&sm.o_free));
+                    ++u;
+                }
+            }
+            if (!ok) record_timeout(args, abort);
+            bulk_wait_group0();  // written out before the CTA leaves
         }
     } else {
         // ===================== softmax / epilogue =====================
@@ -381,25 +476,42 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
         const int wq = warp & 3;        // TMEM lane quarter this warp may access
         const int cq = lane & 3;        // column group within the row's four threads
         const int rA = wq * 32 + sub * 16 + (lane >> 2);
-        const int my_q0 = t == 0 ? q0[0] : q0[1];
-        const int my_nkv = t == 0 ? nkv[0] : nkv[1];
-        const int qA = my_q0 + rA, qB = qA + 8;
         const uint32_t lanes16 = tbase + (static_cast<uint32_t>(wq * 32 + sub * 16) << 16);
         const uint32_t s_addr = lanes16 + static_cast<uint32_t>(t) * Cfg::kSColStride;
         const uint32_t o_addr = lanes16 + Cfg::kOCol0 + t * HD;
         const float sl2 = args.scale_log2;
-        // Per row (A, B): running max in log2 units, this thread's share of the
-        // fp32 row sum (for lse), and a correction that turns the row sum into the
-        // sum of the bf16 weights P V actually used, for the largest weight of each
-        // tile only: that weight's rounding is what biases O when one key
-        // dominates, the other weights' rounding errors average out.
-        float mA = -INFINITY, mB = -INFINITY;
-        uint64_t lA = f2_pack(0.f, 0.f), lB = f2_pack(0.f, 0.f);
-        float lcA = 0.f, lcB = 0.f;
         const uint64_t sl2_pair = f2_pack(sl2, sl2);
         bool ok = true;
-        for (int j = 0; j < my_nkv; ++j) {
-            ok = mbar_wait_warp(smem_u32(&sm.s_full[t]), j & 1, kWaitTimeoutNs, abort);
+        // The running counts are only needed as barrier phases, kept as bits (few
+        // registers stay live across the key loop): bit 0, S_t tiles before the
+        // item (s_full, p_full, o_done); bit 1, O tiles staged before the item by
+        // both Q tiles (o_free); bit 2, at least one staged; bits 4-5, items taken
+        // mod 4 (queue slot and phase).  The item's queue slot is released only at
+        // the end of the item, so its details are read from it again there.
+        unsigned par = 0;
+        while (ok) {
+          const int slot = (par >> 4) & 1;
+          if (!(ok = mbar_wait_warp(smem_u32(&sm.item_full[slot]), (par >> 5) & 1, kWaitTimeoutNs, abort)))
+              break;
+          if (sm.item[slot] < 0) break;
+          int my_q0, my_nkv;
+          {
+              const FwdItem it = fwd_item(args, sm.item[slot]);
+              my_q0 = t == 0 ? it.q0[0] : it.q0[1];
+              my_nkv = t == 0 ? it.nkv[0] : it.nkv[1];
+          }
+          const int qA = my_q0 + rA, qB = qA + 8;
+          // Per row (A, B): running max in log2 units, this thread's share of the
+          // fp32 row sum (for lse), and a correction that turns the row sum into the
+          // sum of the bf16 weights P V actually used, for the largest weight of each
+          // tile only: that weight's rounding is what biases O when one key
+          // dominates, the other weights' rounding errors average out.
+          float mA = -INFINITY, mB = -INFINITY;
+          uint64_t lA = f2_pack(0.f, 0.f), lB = f2_pack(0.f, 0.f);
+          float lcA = 0.f, lcB = 0.f;
+          for (int j = 0; j < my_nkv; ++j) {
+            const unsigned gpar = (par ^ static_cast<unsigned>(j)) & 1u;  // phase of this S_t
+            ok = mbar_wait_warp(smem_u32(&sm.s_full[t]), gpar, kWaitTimeoutNs, abort);
             if (!ok) break;
             tc_fence_after();
             uint32_t sa[32], sb[32];  // keys 0-63 and 64-127 of the tile
@@ -418,12 +530,12 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
 #pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        const int ka = kbase + 8 * i + c, kb = ka + 64;
-                        if (ka >= kendA) sa[4 * i + c] = __float_as_uint(-INFINITY);
-                        if (ka >= kendB) sa[4 * i + 2 + c] = __float_as_uint(-INFINITY);
-                        if (kb >= kendA) sb[4 * i + c] = __float_as_uint(-INFINITY);
-                        if (kb >= kendB) sb[4 * i + 2 + c] = __float_as_uint(-INFINITY);
+                    for (int c2 = 0; c2 < 2; ++c2) {
+                        const int ka = kbase + 8 * i + c2, kb = ka + 64;
+                        if (ka >= kendA) sa[4 * i + c2] = __float_as_uint(-INFINITY);
+                        if (ka >= kendB) sa[4 * i + 2 + c2] = __float_as_uint(-INFINITY);
+                        if (kb >= kendA) sb[4 * i + c2] = __float_as_uint(-INFINITY);
+                        if (kb >= kendB) sb[4 * i + 2 + c2] = __float_as_uint(-INFINITY);
                     }
                 }
             }
@@ -436,11 +548,11 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
 #pragma unroll
             for (int i = 1; i < 15; i += 2) {  // repetitions 1..14 in pairs
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    ma[c] = fmax3(ma[c], __uint_as_float(SR(4 * i + c)),
-                                  __uint_as_float(SR(4 * i + 4 + c)));
-                    mb[c] = fmax3(mb[c], __uint_as_float(SR(4 * i + 2 + c)),
-                                  __uint_as_float(SR(4 * i + 6 + c)));
+                for (int c2 = 0; c2 < 2; ++c2) {
+                    ma[c2] = fmax3(ma[c2], __uint_as_float(SR(4 * i + c2)),
+                                   __uint_as_float(SR(4 * i + 4 + c2)));
+                    mb[c2] = fmax3(mb[c2], __uint_as_float(SR(4 * i + 2 + c2)),
+                                   __uint_as_float(SR(4 * i + 6 + c2)));
                 }
             }
             // repetition 15
@@ -515,9 +627,10 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                 }
                 tmem_st_16x128b_x8(s_addr + hh * 32, pk);
                 if (hh == 0 && any_rescale) {
-                    // O already holds P V of earlier tiles: wait for the latest one,
-                    // then rescale it before any of this tile's P V is issued.
-                    ok = mbar_wait_warp(smem_u32(&sm.o_done[t]), (j - 1) & 1, kWaitTimeoutNs, abort);
+                    // O already holds P V of earlier tiles of this item (a rescale needs
+                    // a finite running max, so j > 0): wait for the latest one, then
+                    // rescale it before any of this tile's P V is issued.
+                    ok = mbar_wait_warp(smem_u32(&sm.o_done[t]), gpar ^ 1u, kWaitTimeoutNs, abort);
                     if (!ok) break;
                     tc_fence_after();
                     const uint64_t aA = f2_pack(alphaA, alphaA), aB = f2_pack(alphaB, alphaB);
@@ -551,60 +664,73 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                 lcA += __uint_as_float(pb << 16) - pxA;
                 lcB += __uint_as_float(pb & 0xffff0000u) - pxB;
             }
-        }
-        if (!ok) {
-            if (lane == 0) record_timeout(args, abort);
-        } else if (my_nkv > 0) {
-            // full row sums across the row's four threads
-            const float2 la = f2_unpack(lA), lb = f2_unpack(lB);
-            float sA = la.x + la.y, sB = lb.x + lb.y;
-            sA += __shfl_xor_sync(0xffffffffu, sA, 1);
-            sB += __shfl_xor_sync(0xffffffffu, sB, 1);
-            sA += __shfl_xor_sync(0xffffffffu, sA, 2);
-            sB += __shfl_xor_sync(0xffffffffu, sB, 2);
-            ok = mbar_wait_warp(smem_u32(&sm.o_done[t]), (my_nkv - 1) & 1, kWaitTimeoutNs, abort);
-            if (ok) {
-                tc_fence_after();
-                const float invA = 1.f / (sA + lcA), invB = 1.f / (sB + lcB);
-                const bool storeA = qA < N, storeB = qB < N;
-                // O rows rA and rB into the tile's Q buffer (free: the tile's last
-                // S MMA finished before its last P V), as 64-column boxes of
-                // 128-byte rows; column 8i + 2cq is 16-byte chunk i % 8 of box i / 8,
-                // at position (i % 8) ^ (row % 8), bytes 4cq.. (rB % 8 == rA % 8)
-                const uint32_t qbuf = smem_u32(sm.q[t]);
+          }
+          if (!ok) break;
+          const FwdItem it = fwd_item(args, sm.item[slot]);
+          // this tile's staging follows tile 0's when both are active
+          const bool after0 = t == 1 && it.nkv[0] > 0;
+          const unsigned prev_staged = ((par >> 2) | (after0 ? 1u : 0u)) & 1u;     // an earlier staging exists
+          const unsigned prev_par = ((par >> 1) ^ (after0 ? 1u : 0u) ^ 1u) & 1u;  // its o_free phase
+          par ^= (static_cast<unsigned>(((it.nkv[0] > 0) + (it.nkv[1] > 0)) & 1) << 1) |
+                 (static_cast<unsigned>(my_nkv) & 1u);
+          par |= 4u;
+          par = (par & 15u) | ((((par >> 4) + 1u) & 3u) << 4);
+          if (my_nkv == 0) {  // inactive tile past the end of the sequence
+              mbar_arrive(smem_u32(&sm.item_empty[slot]));
+              continue;
+          }
+          // full row sums across the row's four threads
+          const float2 la = f2_unpack(lA), lb = f2_unpack(lB);
+          float sA = la.x + la.y, sB = lb.x + lb.y;
+          sA += __shfl_xor_sync(0xffffffffu, sA, 1);
+          sB += __shfl_xor_sync(0xffffffffu, sB, 1);
+          sA += __shfl_xor_sync(0xffffffffu, sA, 2);
+          sB += __shfl_xor_sync(0xffffffffu, sB, 2);
+          // the item's last P V, and the staging buffer back from the previous store
+          if (!(ok = mbar_wait_warp(smem_u32(&sm.o_done[t]), (par & 1u) ^ 1u, kWaitTimeoutNs, abort)))
+              break;
+          if (prev_staged &&
+              !(ok = mbar_wait_warp(smem_u32(&sm.o_free), prev_par, kWaitTimeoutNs, abort)))
+              break;
+          tc_fence_after();
+          const float invA = 1.f / (sA + lcA), invB = 1.f / (sB + lcB);
+          // O rows rA and rB into the staging buffer as 64-column boxes of 128-byte
+          // rows; column 8i + 2cq is 16-byte chunk i % 8 of box i / 8, at position
+          // (i % 8) ^ (row % 8), bytes 4cq.. (rB % 8 == rA % 8)
+          const uint32_t obuf = smem_u32(sm.o);
 #pragma unroll
-                for (int c = 0; c < HD / 32; ++c) {
-                    uint32_t r[16];
-                    tmem_ld_16x256b_x4(o_addr + c * 32, r);
-                    tmem_wait_ld();
-                    reg_fence(r);
+          for (int c = 0; c < HD / 32; ++c) {
+              uint32_t r[16];
+              tmem_ld_16x256b_x4(o_addr + c * 32, r);
+              tmem_wait_ld();
+              reg_fence(r);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const uint32_t wa = pack_bf16x2(__uint_as_float(r[4 * i]) * invA,
-                                                        __uint_as_float(r[4 * i + 1]) * invA);
-                        const uint32_t wb = pack_bf16x2(__uint_as_float(r[4 * i + 2]) * invB,
-                                                        __uint_as_float(r[4 * i + 3]) * invB);
-                        const int ii = c * 4 + i;
-                        const uint32_t off = static_cast<uint32_t>(
-                            (ii / 8) * kBoxBytes + (((ii % 8) ^ (rA & 7)) << 4) + 4 * cq);
-                        st_shared_b32(qbuf + off + static_cast<uint32_t>(rA * 128), wa);
-                        st_shared_b32(qbuf + off + static_cast<uint32_t>((rA + 8) * 128), wb);
-                    }
-                }
-                fence_proxy_async_smem();
-                mbar_arrive(smem_u32(&sm.out_staged[t]));
-                if (cq == 0) {
-                    if (storeA)
-                        args.lse[static_cast<size_t>(bh) * N + qA] =
-                            (mA + __log2f(sA)) * 0.69314718055994531f;
-                    if (storeB)
-                        args.lse[static_cast<size_t>(bh) * N + qB] =
-                            (mB + __log2f(sB)) * 0.69314718055994531f;
-                }
-            } else if (lane == 0) {
-                record_timeout(args, abort);
-            }
+              for (int i = 0; i < 4; ++i) {
+                  const uint32_t wa = pack_bf16x2(__uint_as_float(r[4 * i]) * invA,
+                                                  __uint_as_float(r[4 * i + 1]) * invA);
+                  const uint32_t wb = pack_bf16x2(__uint_as_float(r[4 * i + 2]) * invB,
+                                                  __uint_as_float(r[4 * i + 3]) * invB);
+                  const int ii = c * 4 + i;
+                  const uint32_t off = static_cast<uint32_t>(
+                      (ii / 8) * kBoxBytes + (((ii % 8) ^ (rA & 7)) << 4) + 4 * cq);
+                  st_shared_b32(obuf + off + static_cast<uint32_t>(rA * 128), wa);
+                  st_shared_b32(obuf + off + static_cast<uint32_t>((rA + 8) * 128), wb);
+              }
+          }
+          // the O reads above come before the next item's first P V into O_t, which
+          // waits for this thread's next p_full arrival
+          tc_fence_before();
+          fence_proxy_async_smem();
+          mbar_arrive(smem_u32(&sm.out_staged));
+          if (cq == 0) {
+              if (qA < N)
+                  args.lse[static_cast<size_t>(it.bh) * N + qA] = (mA + __log2f(sA)) * 0.69314718055994531f;
+              if (qB < N)
+                  args.lse[static_cast<size_t>(it.bh) * N + qB] = (mB + __log2f(sB)) * 0.69314718055994531f;
+          }
+          mbar_arrive(smem_u32(&sm.item_empty[slot]));
         }
+        if (!ok && lane == 0) record_timeout(args, abort);
     }
 
     tc_fence_before();
@@ -623,7 +749,13 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    const unsigned grid = static_cast<unsigned>(args.n_qblk) * static_cast<unsigned>(args.BH);
+    const long long items = static_cast<long long>(args.n_qblk) * args.BH;
+    unsigned grid = static_cast<unsigned>(items);
+    if (args.work) {
+        // persistent: one CTA per multiprocessor, work items handed out by a counter
+        if ((e = cudaMemsetAsync(args.work, 0, sizeof(unsigned), stream)) != cudaSuccess) return e;
+        grid = static_cast<unsigned>(items < args.sms ? items : args.sms);
+    }
     fa_fwd_kernel<HD><<<grid, kThreads, smem, stream>>>(tq, tk, tv, to, args);
     return cudaGetLastError();
 }

@@ -41,10 +41,12 @@ struct FwdArgs {
     int BH;
     int N;
     int n_qblk;       // query blocks (256 rows each) per head
-    int group;        // causal launch order: heads per group (heavy blocks first within a group)
+    int group;        // causal item order: heads per group (heavy blocks first within a group)
     int causal;
     float scale_log2; // scale * log2(e)
     int* status;      // device status word
+    unsigned* work;   // work-item counter (zeroed before the launch), or null: one item per CTA
+    int sms;          // multiprocessors of the device (grid of the persistent launch)
 };
 
 // Counters of the persistent backward kernels inside BwdArgs::work, 128 bytes apart.

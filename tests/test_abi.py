@@ -57,12 +57,12 @@ FAKE = 0x100000  # 16-byte aligned, never dereferenced: validation fails first
 
 def test_fwd_argument_errors(lib):
     args = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=1, H=1, N=128, d=64,
-                scale=0.125, causal=0, stream=None)
+                scale=0.125, causal=0, ws=None, ws_bytes=0, stream=None)
 
     def call(**kw):
         a = dict(args, **kw)
         return fa.fa_fwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["N"],
-                         a["d"], a["scale"], a["causal"], a["stream"])
+                         a["d"], a["scale"], a["causal"], a["ws"], a["ws_bytes"], a["stream"])
 
     assert call(q=None) == fa.FA_ERR_INVALID_ARG
     assert call(lse=None) == fa.FA_ERR_INVALID_ARG
@@ -78,6 +78,11 @@ def test_fwd_argument_errors(lib):
     assert call(q=FAKE + 8) == fa.FA_ERR_MISALIGNED
     assert call(o=FAKE + 2) == fa.FA_ERR_MISALIGNED
     assert call(lse=FAKE + 2) == fa.FA_ERR_MISALIGNED
+    # the optional work-counter workspace: 256-byte aligned, at least the size asked for
+    assert fa.fa_fwd_workspace_size(1, 1, 128, 64) == 256
+    assert fa.fa_fwd_workspace_size(0, 1, 128, 64) == 0
+    assert call(ws=FAKE + 16, ws_bytes=256) == fa.FA_ERR_WORKSPACE
+    assert call(ws=FAKE, ws_bytes=255) == fa.FA_ERR_WORKSPACE
 
 
 def test_bwd_argument_errors(lib):

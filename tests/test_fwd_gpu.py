@@ -138,6 +138,20 @@ def test_many_heads_short_rows():
         check_lse(to_np(lse).reshape(l_ref.shape), l_ref, "many heads")
 
 
+@pytest.mark.parametrize("N,d,H", [(300, 128, 24), (1000, 64, 24), (4096, 128, 8)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_persistent_matches_one_item_per_cta(N, d, H, causal):
+    """With the work counter one CTA per SM runs many (head, query block) items
+    back to back; without it each CTA runs one.  Every item is computed by the
+    same code in the same order, so O and lse are bitwise equal."""
+    inp = wl.make_inputs(wl.WORKLOADS["single_head_256"], B=2, H=H, N=N, d=d, seed=N + d + causal)
+    q, k, v = (inp[n].to(DEV) for n in ("q", "k", "v"))
+    o1, l1 = fa.forward(q, k, v, causal=causal)
+    o2, l2 = fa.forward(q, k, v, causal=causal, workspace=False)
+    fa.sync_status()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
 def test_large_scores_dynamic_range():
     """Scores of magnitude ~100: the running max moves by far more than the
     rescale threshold, many times per row."""
@@ -225,6 +239,6 @@ def test_device_argument_errors():
     lse = torch.empty(1, 1, 128, dtype=torch.float32, device=DEV)
     h = torch.cuda.current_stream().cuda_stream
     rc = fa.fa_fwd(q.data_ptr() + 2, q.data_ptr(), q.data_ptr(), q.data_ptr(), lse.data_ptr(),
-                   1, 1, 128, 64, 0.125, 0, h)
+                   1, 1, 128, 64, 0.125, 0, None, 0, h)
     assert rc == fa.FA_ERR_MISALIGNED
     assert fa.fa_sync_status(h) == fa.FA_OK

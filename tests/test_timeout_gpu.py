@@ -33,7 +33,7 @@ def fault_lib(tmp_path_factory):
                           extra_flags=["-DFA_FAULT_INJECT=1", "-DFA_WAIT_TIMEOUT_NS=200000000ull"])
     lib = ctypes.CDLL(path)
     P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
-    lib.fa_fwd.argtypes = [P, P, P, P, P, I, I, I, I, F, I, P]
+    lib.fa_fwd.argtypes = [P, P, P, P, P, I, I, I, I, F, I, P, Z, P]
     lib.fa_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, F, I, P, Z, P]
     lib.fa_sync_status.argtypes = [P]
     for f in (lib.fa_fwd, lib.fa_bwd, lib.fa_sync_status):
@@ -62,8 +62,9 @@ def test_forward_wait_runs_out_and_reports(fault_lib):
     lse = torch.zeros(1, 1, 200, dtype=torch.float32, device=DEV)
     h = torch.cuda.current_stream().cuda_stream
     t0 = time.time()
+    ws = torch.empty(256, dtype=torch.uint8, device=DEV)  # persistent launch
     rc = fault_lib.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                          1, 1, 200, 128, 0.088, 1, h)
+                          1, 1, 200, 128, 0.088, 1, ws.data_ptr(), ws.numel(), h)
     assert rc == fa.FA_OK  # the launch itself succeeds
     assert fault_lib.fa_sync_status(h) == fa.FA_ERR_DEVICE_TIMEOUT
     assert time.time() - t0 < 30

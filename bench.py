@@ -1,6 +1,6 @@
 """Benchmark: exact attention fwd+bwd on GB300, TFLOP/s and % of dense BF16 peak.
 
-One step = the whole path on one batch: fa_fwd (O, lse) then fa_bwd (prep ->
+One step = the whole path on one batch: fa_fwd_ws (O, lse) then fa_bwd (prep ->
 D, main -> dK, dV, dq -> dQ) on the workload B=4 H=16 N=4096 d=128, causal,
 bf16 inputs resident in HBM.  FLOPs per step follow the convention
 4*B*H*N^2*d for the forward, halved for causal, and 2.5x that for the
@@ -281,8 +281,8 @@ def run_gpu(args, world, rank, local):
     def step(ev=None):
         if ev:
             ev[0].record(stream)
-        check(fa.fa_fwd(P(q), P(k), P(v), P(o), P(lse), B, H, N, d, scale, 1, P(fws), fws.numel(), h),
-              "fa_fwd")
+        check(fa.fa_fwd_ws(P(q), P(k), P(v), P(o), P(lse), B, H, N, d, scale, 1, P(fws), fws.numel(),
+                           h), "fa_fwd_ws")
         if ev:
             ev[1].record(stream)
         check(fa.fa_bwd_prep(P(o), P(do), P(lse), B, H, N, d, P(ws), ws.numel(), h), "fa_bwd_prep")

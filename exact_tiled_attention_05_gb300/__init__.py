@@ -24,7 +24,7 @@ FA_ERR_CUDA = 5
 FA_ERR_DEVICE_TIMEOUT = 6
 
 EXPORTED = (
-    "fa_fwd", "fa_fwd_workspace_size", "fa_bwd", "fa_bwd_workspace_size", "fa_bwd_prep", "fa_bwd_main",
+    "fa_fwd", "fa_fwd_ws", "fa_fwd_workspace_size", "fa_bwd", "fa_bwd_workspace_size", "fa_bwd_prep", "fa_bwd_main",
     "fa_bwd_dq", "fa_bwd_noalloc", "fa_fp8_workspace_size", "fa_fp8_quantize", "fa_fwd_fp8",
     "fa_sync_status", "fa_status_string", "fa_version",
 )
@@ -53,7 +53,8 @@ def load_library(path: str = LIB_PATH):
     lib = ctypes.CDLL(path)
     P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     sig = {
-        "fa_fwd": ([P, P, P, P, P, I, I, I, I, F, I, P, Z, P], I),
+        "fa_fwd": ([P, P, P, P, P, I, I, I, I, F, I, P], I),
+        "fa_fwd_ws": ([P, P, P, P, P, I, I, I, I, F, I, P, Z, P], I),
         "fa_fwd_workspace_size": ([I, I, I, I], Z),
         "fa_bwd_workspace_size": ([I, I, I, I], Z),
         "fa_bwd": ([P, P, P, P, P, P, P, P, P, I, I, I, I, F, I, P, Z, P], I),
@@ -80,8 +81,13 @@ def load_library(path: str = LIB_PATH):
 # one-to-one wrappers of the C ABI (pointers as Python ints)
 # ---------------------------------------------------------------------------
 
-def fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, ws, ws_bytes, stream):
-    return load_library().fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, ws, ws_bytes, stream)
+def fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, stream):
+    return load_library().fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, stream)
+
+
+def fa_fwd_ws(q, k, v, o, lse, B, H, N, d, scale, causal, ws, ws_bytes, stream):
+    return load_library().fa_fwd_ws(q, k, v, o, lse, B, H, N, d, scale, causal, ws, ws_bytes,
+                                    stream)
 
 
 def fa_fwd_workspace_size(B, H, N, d):
@@ -193,10 +199,10 @@ def _check_qkv(*ts):
 
 def forward(q, k, v, scale=None, causal=False, out=None, lse=None, workspace=None, stream=None):
     """O, lse = attention(q, k, v).  q, k, v: bf16 [B, H, N, d] on the GPU.
-    Returns (o bf16 [B,H,N,d], lse fp32 [B,H,N]).  `workspace` (uint8 CUDA
-    tensor of fa_fwd_workspace_size bytes) holds the kernel's work counter; one
-    is allocated when none is given.  workspace=False runs without one (one CTA
-    per work item)."""
+    Returns (o bf16 [B,H,N,d], lse fp32 [B,H,N]).  Runs fa_fwd_ws: `workspace`
+    (uint8 CUDA tensor of fa_fwd_workspace_size bytes) holds the kernel's work
+    counter, and one is allocated when none is given.  workspace=False runs
+    fa_fwd instead (no workspace, one CTA per work item, same results)."""
     torch = _torch()
     B, H, N, d = _check_qkv(q, k, v)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
@@ -211,9 +217,13 @@ def forward(q, k, v, scale=None, causal=False, out=None, lse=None, workspace=Non
         workspace = torch.empty(int(fa_fwd_workspace_size(B, H, N, d)), dtype=torch.uint8,
                                 device=q.device)
         _keep_for_stream(workspace, stream)
-    ws_ptr, ws_bytes = (0, 0) if workspace is False else (workspace.data_ptr(), workspace.numel())
-    rc = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
-                B, H, N, d, scale, int(bool(causal)), ws_ptr, ws_bytes, _stream_handle(stream))
+    if workspace is False:
+        rc = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                    B, H, N, d, scale, int(bool(causal)), _stream_handle(stream))
+    else:
+        rc = fa_fwd_ws(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                       B, H, N, d, scale, int(bool(causal)), workspace.data_ptr(), workspace.numel(),
+                       _stream_handle(stream))
     _check(rc, "fa_fwd")
     return out, lse
 

@@ -284,7 +284,12 @@ size_t fa_fwd_workspace_size(int B, int H, int N, int d) {
 }
 
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
-           int d, float scale, int causal, void* workspace, size_t workspace_bytes, void* stream) {
+           int d, float scale, int causal, void* stream) {
+    return fa_fwd_ws(q, k, v, o, lse, B, H, N, d, scale, causal, nullptr, 0, stream);
+}
+
+int fa_fwd_ws(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+              int d, float scale, int causal, void* workspace, size_t workspace_bytes, void* stream) {
     if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
     int rc = check_shape(B, H, N, d, scale, causal);
     if (rc) return rc;

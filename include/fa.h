@@ -53,20 +53,26 @@ typedef enum {
  * softmax with a running max m and running sum l per row, unnormalised output
  * accumulator rescaled when the max moves, one normalisation O = acc / l at the
  * end, lse = m + ln l ("FlashAttention 1–4" §"FlashAttention (v1)" recurrence;
- * "07 GPU、资源估算与 FlashAttention" §7.8).  workspace: NULL, or caller-owned
- * device memory of at least fa_fwd_workspace_size() bytes, 256-byte aligned
- * (contents on entry do not matter), that holds a work counter: with it one
- * CTA per multiprocessor takes (head, 256-row query block) items until none
- * are left, without it each CTA takes one item (same results, slower).  Two
- * calls that overlap on the GPU must not share a workspace.  A workspace that
- * is too small or misaligned returns FA_ERR_WORKSPACE.  `stream` is a
- * cudaStream_t. */
+ * "07 GPU、资源估算与 FlashAttention" §7.8).  Each CTA computes one (head,
+ * 256-row query block) work item; fa_fwd_ws below gives the same results
+ * faster with a small workspace.  `stream` is a cudaStream_t. */
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
-           int B, int H, int N, int d, float scale, int causal, void* workspace,
-           size_t workspace_bytes, void* stream);
+           int B, int H, int N, int d, float scale, int causal, void* stream);
 
-/* Bytes of device workspace fa_fwd uses: a 256-byte slot for its work counter
- * (the sizes do not change it; 0 for invalid sizes). */
+/* fa_fwd with a workspace holding a work counter: one CTA per multiprocessor
+ * takes (head, 256-row query block) items until none are left, so the start-up
+ * and epilogue of one item overlap the work of the next.  workspace:
+ * caller-owned device memory of at least fa_fwd_workspace_size() bytes,
+ * 256-byte aligned, contents on entry irrelevant; two calls that overlap on the
+ * GPU must not share one.  NULL behaves as fa_fwd.  A workspace that is too
+ * small or misaligned returns FA_ERR_WORKSPACE.  Results are bitwise equal to
+ * fa_fwd's. */
+int fa_fwd_ws(const void* q, const void* k, const void* v, void* o, float* lse,
+              int B, int H, int N, int d, float scale, int causal, void* workspace,
+              size_t workspace_bytes, void* stream);
+
+/* Bytes of device workspace fa_fwd_ws uses: a 256-byte slot for its work
+ * counter (the sizes do not change it; 0 for invalid sizes). */
 size_t fa_fwd_workspace_size(int B, int H, int N, int d);
 
 /* Bytes of device workspace fa_bwd needs for these sizes: two fp32 row

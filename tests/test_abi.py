@@ -61,8 +61,11 @@ def test_fwd_argument_errors(lib):
 
     def call(**kw):
         a = dict(args, **kw)
-        return fa.fa_fwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["N"],
-                         a["d"], a["scale"], a["causal"], a["ws"], a["ws_bytes"], a["stream"])
+        if a["ws"] is None:
+            return fa.fa_fwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["N"],
+                             a["d"], a["scale"], a["causal"], a["stream"])
+        return fa.fa_fwd_ws(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["N"],
+                            a["d"], a["scale"], a["causal"], a["ws"], a["ws_bytes"], a["stream"])
 
     assert call(q=None) == fa.FA_ERR_INVALID_ARG
     assert call(lse=None) == fa.FA_ERR_INVALID_ARG
@@ -83,6 +86,7 @@ def test_fwd_argument_errors(lib):
     assert fa.fa_fwd_workspace_size(0, 1, 128, 64) == 0
     assert call(ws=FAKE + 16, ws_bytes=256) == fa.FA_ERR_WORKSPACE
     assert call(ws=FAKE, ws_bytes=255) == fa.FA_ERR_WORKSPACE
+    assert call(ws=FAKE, ws_bytes=256, q=None) == fa.FA_ERR_INVALID_ARG  # checked before the workspace
 
 
 def test_bwd_argument_errors(lib):

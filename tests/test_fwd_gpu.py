@@ -239,6 +239,6 @@ def test_device_argument_errors():
     lse = torch.empty(1, 1, 128, dtype=torch.float32, device=DEV)
     h = torch.cuda.current_stream().cuda_stream
     rc = fa.fa_fwd(q.data_ptr() + 2, q.data_ptr(), q.data_ptr(), q.data_ptr(), lse.data_ptr(),
-                   1, 1, 128, 64, 0.125, 0, None, 0, h)
+                   1, 1, 128, 64, 0.125, 0, h)
     assert rc == fa.FA_ERR_MISALIGNED
     assert fa.fa_sync_status(h) == fa.FA_OK

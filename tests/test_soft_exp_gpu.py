@@ -26,8 +26,8 @@ def soft_lib(tmp_path_factory):
                           extra_flags=["-DFA_SOFT_EXP_EVERY=2"])
     lib = ctypes.CDLL(path)
     P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
-    lib.fa_fwd.argtypes = [P, P, P, P, P, I, I, I, I, F, I, P, Z, P]
-    lib.fa_fwd.restype = I
+    lib.fa_fwd_ws.argtypes = [P, P, P, P, P, I, I, I, I, F, I, P, Z, P]
+    lib.fa_fwd_ws.restype = I
     lib.fa_sync_status.argtypes = [P]
     lib.fa_sync_status.restype = I
     return lib
@@ -40,8 +40,8 @@ def run(lib, inp, causal, scale):
     lse = torch.empty(B, H, N, dtype=torch.float32, device=DEV)
     h = torch.cuda.current_stream().cuda_stream
     ws = torch.empty(256, dtype=torch.uint8, device=DEV)
-    assert lib.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                      B, H, N, d, scale, int(causal), ws.data_ptr(), ws.numel(), h) == 0
+    assert lib.fa_fwd_ws(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                         B, H, N, d, scale, int(causal), ws.data_ptr(), ws.numel(), h) == 0
     assert lib.fa_sync_status(h) == 0
     return to_np(o).reshape(B * H, N, d), to_np(lse).reshape(B * H, N)
 

@@ -33,10 +33,11 @@ def fault_lib(tmp_path_factory):
                           extra_flags=["-DFA_FAULT_INJECT=1", "-DFA_WAIT_TIMEOUT_NS=200000000ull"])
     lib = ctypes.CDLL(path)
     P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
-    lib.fa_fwd.argtypes = [P, P, P, P, P, I, I, I, I, F, I, P, Z, P]
+    lib.fa_fwd.argtypes = [P, P, P, P, P, I, I, I, I, F, I, P]
+    lib.fa_fwd_ws.argtypes = [P, P, P, P, P, I, I, I, I, F, I, P, Z, P]
     lib.fa_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, F, I, P, Z, P]
     lib.fa_sync_status.argtypes = [P]
-    for f in (lib.fa_fwd, lib.fa_bwd, lib.fa_sync_status):
+    for f in (lib.fa_fwd, lib.fa_fwd_ws, lib.fa_bwd, lib.fa_sync_status):
         f.restype = I
     return lib
 
@@ -55,16 +56,22 @@ def _normal_library_still_works():
     check_lse(to_np(lse).reshape(l_ref.shape), l_ref, "after timeout")
 
 
-def test_forward_wait_runs_out_and_reports(fault_lib):
+@pytest.mark.parametrize("persistent", [True, False])
+def test_forward_wait_runs_out_and_reports(fault_lib, persistent):
     inp = _inputs(200, 128, 1)
     q, k, v = (inp[n].to(DEV) for n in ("q", "k", "v"))
     o = torch.zeros_like(q)
     lse = torch.zeros(1, 1, 200, dtype=torch.float32, device=DEV)
     h = torch.cuda.current_stream().cuda_stream
     t0 = time.time()
-    ws = torch.empty(256, dtype=torch.uint8, device=DEV)  # persistent launch
-    rc = fault_lib.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                          1, 1, 200, 128, 0.088, 1, ws.data_ptr(), ws.numel(), h)
+    if persistent:  # fa_fwd_ws: one CTA per SM with a work counter
+        ws = torch.empty(256, dtype=torch.uint8, device=DEV)
+        rc = fault_lib.fa_fwd_ws(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                 lse.data_ptr(), 1, 1, 200, 128, 0.088, 1, ws.data_ptr(),
+                                 ws.numel(), h)
+    else:
+        rc = fault_lib.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                              lse.data_ptr(), 1, 1, 200, 128, 0.088, 1, h)
     assert rc == fa.FA_OK  # the launch itself succeeds
     assert fault_lib.fa_sync_status(h) == fa.FA_ERR_DEVICE_TIMEOUT
     assert time.time() - t0 < 30

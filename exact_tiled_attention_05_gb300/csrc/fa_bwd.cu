@@ -87,9 +87,12 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const BwdArgs a) {
 // when they finish dS^T(i).  Q_i is read until dK(i), dO_i only until dV(i),
 // so Q has one more slot than dO.
 // Epilogue: the compute warps stage bf16 dV and scale * dK, 128-byte
-// swizzled, in two Q slots (free once the last dK has read them) and warp 3
-// writes them out with TMA tile stores (per-thread row stores of a 128-row
-// tile measured ~12 B/clk, the CTA's slowest phase).
+// swizzled, in the dO and Q slots of the item's last query tile (free once its
+// dV and dK are done) and warp 3 writes them out with TMA tile stores
+// (per-thread row stores of a 128-row tile measured ~12 B/clk, the CTA's
+// slowest phase), handing the slots back to the dO and Q rings once the copies
+// have read them.  K and V are released after the item's last S^T and dP^T,
+// so the next item's K and V load while its last query tile is processed.
 // Roles: warp 0 TMA loads, warp 1 MMA, warp 2 TMEM allocation, warp 3 TMA
 // stores, warps 4-7 / 8-11 compute for query columns 0-63 / 64-127 of each tile.
 // ---------------------------------------------------------------------------
@@ -121,11 +124,11 @@ struct alignas(1024) BwdSmem {
     int item[2];                             // work items published by the loader (-1: none left)
     uint64_t item_full[2], item_empty[2];    // per queue slot: written / read by every role
     uint64_t kv_full;                        // K_j and V_j of the item landed (once per item)
-    uint64_t k_free, v_free;                 // staged dK / dV read out of the K / V buffer (per item)
+    uint64_t k_free, v_free;                 // the item's last S^T / dP^T has read K / V (per item)
     uint64_t q_full[BwdCfg<HD>::kQSlots];    // Q tile and its lse * log2(e) landed
-    uint64_t q_empty[BwdCfg<HD>::kQSlots];   // committed after dK(i)
+    uint64_t q_empty[BwdCfg<HD>::kQSlots];   // after dK(i); an item's last slot after its dK store
     uint64_t do_full[BwdCfg<HD>::kDoSlots];  // dO tile and its D landed
-    uint64_t do_empty[BwdCfg<HD>::kDoSlots]; // committed after dV(i)
+    uint64_t do_empty[BwdCfg<HD>::kDoSlots]; // after dV(i); an item's last slot after its dV store
     uint64_t p_ready[2];  // P^T for each thread's queries 0-31, then 32-63
     uint64_t s_full, dp_full, ds_ready, dkdv_done, drain;
     uint64_t out_staged;  // every compute thread has staged its dV / dK row (per item)
@@ -351,6 +354,7 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                 tc_fence_after();
                 gemm_kk(Cfg::kS, k_addr, smem_u32(sm.q[g % Cfg::kQSlots]));
                 umma_commit(smem_u32(&sm.s_full));
+                if (niter == 1) umma_commit(smem_u32(&sm.k_free));  // the item's last S^T read K
                 for (int it = 0; ok && it < niter; ++it, ++g) {
                     const int qs = g % Cfg::kQSlots, ds = g % Cfg::kDoSlots;
                     const uint32_t q_addr = smem_u32(sm.q[qs]), do_addr = smem_u32(sm.dout[ds]);
@@ -361,6 +365,7 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                     tc_fence_after();
                     gemm_kk(Cfg::kDP, v_addr, do_addr);
                     umma_commit(smem_u32(&sm.dp_full));
+                    if (it + 1 == niter) umma_commit(smem_u32(&sm.v_free));  // the item's last dP^T read V
                     // dV += P^T dO in two parts: queries {0-31, 64-95} (k-steps 0, 1, 4, 5),
                     // each thread's first half of P^T, then {32-63, 96-127}.  The first of
                     // an item overwrites dV: the previous item's dV was read out of TMEM
@@ -379,7 +384,8 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                         }
                     }
                     if (!ok) break;
-                    umma_commit(smem_u32(&sm.do_empty[ds]));  // dO_i read
+                    // dO_i read; the item's last dO slot is released by the dV store
+                    if (it + 1 < niter) umma_commit(smem_u32(&sm.do_empty[ds]));
                     // S^T(i+1) over P^T(i): dV(i) was issued before it.
                     if (it + 1 < niter) {
                         const int qs1 = (g + 1) % Cfg::kQSlots;
@@ -389,11 +395,13 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                         tc_fence_after();
                         gemm_kk(Cfg::kS, k_addr, smem_u32(sm.q[qs1]));
                         umma_commit(smem_u32(&sm.s_full));
+                        if (it + 2 == niter) umma_commit(smem_u32(&sm.k_free));  // last S^T read K
                     }
                     if (!(ok = mbar_wait(smem_u32(&sm.ds_ready), g & 1, kWaitTimeoutNs, abort))) break;
                     tc_fence_after();
                     gemm_tmem_a(Cfg::kDK, Cfg::kDP, q_addr, it > 0);  // dK += dS^T Q
-                    umma_commit(smem_u32(&sm.q_empty[qs]));            // Q_i read
+                    // Q_i read; the item's last Q slot is released by the dK store
+                    if (it + 1 < niter) umma_commit(smem_u32(&sm.q_empty[qs]));
                 }
                 if (ok) umma_commit(smem_u32(&sm.dkdv_done));  // this item's dK, dV complete
             }
@@ -404,13 +412,15 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         }
     } else if (warp == 3) {
         // ===================== dK / dV stores =====================
-        // Per item: the staged dK (in the K buffer) and dV (in the V buffer) go out
-        // with TMA tile stores, as two bulk groups; each buffer is handed back to
-        // the loader as soon as its group has been read out of shared memory.
+        // Per item: the staged dV (in the dO slot of the item's last query tile) and
+        // dK (in its Q slot) go out with TMA tile stores, as two bulk groups; each
+        // slot goes back to its ring as soon as its group has been read out of
+        // shared memory (dV first: the dO ring has fewer slots).
         if (elect_one()) {
             tma_prefetch_desc(&tdk);
             tma_prefetch_desc(&tdv);
             bool ok = true;
+            int g = 0;  // running query-tile count, as in the MMA warp
             for (int k = 0; ok; ++k) {
                 const int slot = k & 1;
                 if (!(ok = mbar_wait(smem_u32(&sm.item_full[slot]), (k >> 1) & 1, kWaitTimeoutNs, abort)))
@@ -420,17 +430,19 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                 if (item < 0) break;
                 int bh, j;
                 dkdv_item(a, item, bh, j);
+                g += nq - (a.causal ? j : 0);
+                const int qs = (g - 1) % Cfg::kQSlots, ds = (g - 1) % Cfg::kDoSlots;
                 if (!(ok = mbar_wait(smem_u32(&sm.out_staged), k & 1, kWaitTimeoutNs, abort))) break;
                 for (int b = 0; b < Cfg::kBoxes; ++b)
-                    tma_store_3d(&tdk, smem_u32(sm.k) + b * kBBox, b * 64, j * 128, bh);
+                    tma_store_3d(&tdv, smem_u32(sm.dout[ds]) + b * kBBox, b * 64, j * 128, bh);
                 bulk_commit_group();
                 for (int b = 0; b < Cfg::kBoxes; ++b)
-                    tma_store_3d(&tdv, smem_u32(sm.v) + b * kBBox, b * 64, j * 128, bh);
+                    tma_store_3d(&tdk, smem_u32(sm.q[qs]) + b * kBBox, b * 64, j * 128, bh);
                 bulk_commit_group();
                 bulk_wait_group_read<1>();
-                mbar_arrive(smem_u32(&sm.k_free));
+                mbar_arrive(smem_u32(&sm.do_empty[ds]));
                 bulk_wait_group_read<0>();
-                mbar_arrive(smem_u32(&sm.v_free));
+                mbar_arrive(smem_u32(&sm.q_empty[qs]));
             }
             if (!ok) bwd_timeout(a, abort);
             bulk_wait_group0();  // written out before the CTA leaves
@@ -562,14 +574,14 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
           tc_fence_after();
           {
                 // this thread's row of columns [wg * d/2, (wg + 1) * d/2) of dV (into
-                // the V buffer) and dK (into the K buffer), free since every MMA of the
-                // item is done: 64-column boxes of 128-byte rows, 16-byte chunk c of
-                // row r at position c ^ (r % 8)
+                // the dO slot of the item's last query tile) and dK (into its Q slot),
+                // free since every MMA of the item is done: 64-column boxes of 128-byte
+                // rows, 16-byte chunk c of row r at position c ^ (r % 8)
                 constexpr int kHalf = HD / 2;
                 const int col0 = wg * kHalf;
                 const uint32_t row_off = static_cast<uint32_t>((col0 / 64) * kBBox + row * 128);
-                const uint32_t dv_row = smem_u32(sm.v) + row_off;
-                const uint32_t dk_row = smem_u32(sm.k) + row_off;
+                const uint32_t dv_row = smem_u32(sm.dout[(g - 1) % Cfg::kDoSlots]) + row_off;
+                const uint32_t dk_row = smem_u32(sm.q[(g - 1) % Cfg::kQSlots]) + row_off;
 #pragma unroll 1
                 for (int c = 0; c < kHalf; c += 32) {
                     uint32_t rv[32], rk[32];
@@ -594,8 +606,7 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                     }
                 }
                 // the TMEM reads above come before the next item's first dV / dK, which
-                // can only be issued after these rows were stored out (barrier chain
-                // out_staged -> k_free -> kv_full)
+                // wait for this thread's next p_ready / ds_ready arrivals
                 tc_fence_before();
                 fence_proxy_async_smem();
                 mbar_arrive(smem_u32(&sm.out_staged));

@@ -55,6 +55,20 @@ int current_sms() {
 
 int clampi(int x, int lo, int hi) { return x < lo ? lo : (x > hi ? hi : x); }
 
+int ceil_pow2(int x) {
+    int p = 1;
+    while (p < x && p < (1 << 30)) p <<= 1;
+    return p;
+}
+
+// Heads in the last group of a causal work order (see grouped_item): at least
+// 3 * sms / nblk, so that the group's work spread over the SMs lasts about 1.5
+// times its heaviest item (nblk blocks of a head hold ~nblk^2 / 2 tiles).
+int last_group(int sms, int nblk, int group, int BH) {
+    const int need = (3 * sms + nblk - 1) / nblk;
+    return clampi(group > ceil_pow2(need) ? group : ceil_pow2(need), 1, BH);
+}
+
 // Largest power of two <= x (x >= 1).
 int floor_pow2(int x) {
     int p = 1;
@@ -228,6 +242,8 @@ int bwd_common(BwdArgs& a, int B, int H, int N, int d, float scale, int causal, 
     // kernel: about two waves, as the forward
     a.group = clampi(floor_pow2(clampi((current_sms() * 9 / 10) / a.n_kblk, 1, 1 << 20)), 1, a.BH);
     a.group_dq = clampi(floor_pow2(clampi((2 * current_sms()) / a.n_kblk, 1, 1 << 20)), 1, a.BH);
+    a.group_last = last_group(current_sms(), a.n_kblk, a.group, a.BH);
+    a.group_dq_last = last_group(current_sms(), a.n_kblk, a.group_dq, a.BH);
     a.sms = current_sms();
     a.scale = scale;
     a.scale_log2 = scale * 1.4426950408889634f;
@@ -314,6 +330,7 @@ int fa_fwd_ws(const void* q, const void* k, const void* v, void* o, float* lse, 
     // about two waves of CTAs per head group, rounded down to a power of two
     // (measured: 8 heads at N = 8192, 16 at N = 4096)
     a.group = clampi(floor_pow2(clampi((2 * current_sms()) / a.n_qblk, 1, 1 << 20)), 1, BH);
+    a.group_last = last_group(current_sms(), a.n_qblk, a.group, BH);
     a.causal = causal;
     a.scale_log2 = scale * 1.4426950408889634f;
     a.work = static_cast<unsigned*>(workspace);

@@ -149,17 +149,12 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
         : "memory");
 }
 
-// Work item t (launch order) -> (head, key block).  Causal: groups of a.group
-// heads; inside a group the key blocks with the most query tiles (small j)
-// come first.  Keeping few heads in flight keeps their Q and dO in L2.
+// Work item t (fetch order) -> (head, key block).  Causal: head groups as in
+// grouped_item; inside a group the key blocks with the most query tiles (small
+// j) come first.  Keeping few heads in flight keeps their Q and dO in L2.
 __device__ __forceinline__ void dkdv_item(const BwdArgs& a, int t, int& bh, int& j) {
     if (a.causal) {
-        const int grp = t / (a.group * a.n_kblk);
-        const int first = grp * a.group;
-        const int gc = min(a.group, a.BH - first);
-        const int r = t - grp * a.group * a.n_kblk;
-        j = r / gc;
-        bh = first + r % gc;
+        grouped_item(t, a.n_kblk, a.BH, a.group, a.group_last, bh, j);
     } else {
         bh = t / a.n_kblk;
         j = t % a.n_kblk;

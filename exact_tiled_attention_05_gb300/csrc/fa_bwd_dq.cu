@@ -90,18 +90,15 @@ struct alignas(1024) DqSmem {
 static_assert(sizeof(DqSmem<128>) <= 232448, "dQ kernel d=128 shared memory exceeds 227 KB");
 static_assert(sizeof(DqSmem<64>) <= 232448, "dQ kernel d=64 shared memory exceeds 227 KB");
 
-// Work item t (fetch order) -> (head, query tile).  Causal: groups of
-// a.group_dq heads; inside a group the query tiles with the most key tiles
-// (large i) come first.
+// Work item t (fetch order) -> (head, query tile).  Causal: head groups as in
+// grouped_item; inside a group the query tiles with the most key tiles (large
+// i) come first.
 __device__ __forceinline__ void dq_item(const BwdArgs& a, int t, int& bh, int& i) {
     const int nq = a.n_kblk;
     if (a.causal) {
-        const int grp = t / (a.group_dq * nq);
-        const int first = grp * a.group_dq;
-        const int gc = min(a.group_dq, a.BH - first);
-        const int r = t - grp * a.group_dq * nq;
-        i = nq - 1 - r / gc;
-        bh = first + r % gc;
+        int rank;
+        grouped_item(t, nq, a.BH, a.group_dq, a.group_dq_last, bh, rank);
+        i = nq - 1 - rank;
     } else {
         bh = t / nq;
         i = t % nq;

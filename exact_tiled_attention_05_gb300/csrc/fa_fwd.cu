@@ -185,12 +185,9 @@ __device__ __forceinline__ FwdItem fwd_item(const FwdArgs& a, int t) {
     FwdItem it;
     int qb;
     if (a.causal) {
-        const int grp = t / (a.group * a.n_qblk);
-        const int first = grp * a.group;
-        const int gc = min(a.group, a.BH - first);
-        const int r = t - grp * a.group * a.n_qblk;
-        qb = a.n_qblk - 1 - r / gc;
-        it.bh = first + r % gc;
+        int rank;
+        grouped_item(t, a.n_qblk, a.BH, a.group, a.group_last, it.bh, rank);
+        qb = a.n_qblk - 1 - rank;
     } else {
         it.bh = t / a.n_qblk;
         qb = t % a.n_qblk;

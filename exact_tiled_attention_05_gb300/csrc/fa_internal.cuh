@@ -42,12 +42,38 @@ struct FwdArgs {
     int N;
     int n_qblk;       // query blocks (256 rows each) per head
     int group;        // causal item order: heads per group (heavy blocks first within a group)
+    int group_last;   // heads in the last group (at least `group`)
     int causal;
     float scale_log2; // scale * log2(e)
     int* status;      // device status word
     unsigned* work;   // work-item counter (zeroed before the launch), or null: one item per CTA
     int sms;          // multiprocessors of the device (grid of the persistent launch)
 };
+
+// Causal work order of the persistent kernels: heads in groups of `group`
+// (a few heads' K/V or Q/dO stay in L2), the last group of `group_last` heads;
+// inside a group the heaviest block of every head first, then the next, and so
+// on.  The last group is larger so that its work, spread over all SMs, outlasts
+// its heaviest items, which then finish with the rest instead of after it.
+// Item t -> head bh and block rank (0 = heaviest).
+__device__ __forceinline__ void grouped_item(int t, int nblk, int BH, int group, int group_last,
+                                             int& bh, int& rank) {
+    const int n_reg = BH - group_last;  // heads in the regular groups
+    const int t_reg = n_reg * nblk;
+    int first, gc, r;
+    if (t < t_reg) {
+        const int grp = t / (group * nblk);
+        first = grp * group;
+        gc = min(group, n_reg - first);
+        r = t - grp * group * nblk;
+    } else {
+        first = n_reg;
+        gc = group_last;
+        r = t - t_reg;
+    }
+    rank = r / gc;
+    bh = first + r % gc;
+}
 
 // Counters of the persistent backward kernels inside BwdArgs::work, 128 bytes apart.
 constexpr int kWorkDkdv = 0;
@@ -72,8 +98,10 @@ struct BwdArgs {
     int BH;
     int N;
     int n_kblk;       // 128-row key blocks per head (= 128-row query blocks)
-    int group;        // causal launch order of the dK/dV kernel: heads per group
-    int group_dq;     // causal launch order of the dQ kernel: heads per group
+    int group;        // causal item order of the dK/dV kernel: heads per group
+    int group_last;   //   heads in its last group (at least `group`)
+    int group_dq;     // causal item order of the dQ kernel: heads per group
+    int group_dq_last;//   heads in its last group
     int causal;
     float scale;
     float scale_log2;

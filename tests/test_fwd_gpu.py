@@ -152,6 +152,30 @@ def test_persistent_matches_one_item_per_cta(N, d, H, causal):
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
+def test_persistent_calls_on_two_streams():
+    """Two persistent forwards at once on two streams, each with its own work
+    counter: the same bits as the calls one after the other."""
+    w = wl.WORKLOADS["single_head_256"]
+    a_in = wl.make_inputs(w, B=2, H=24, N=1000, d=128, seed=61)
+    b_in = wl.make_inputs(w, B=2, H=24, N=1000, d=128, seed=62)
+    qa, ka, va = (a_in[n].to(DEV) for n in ("q", "k", "v"))
+    qb, kb, vb = (b_in[n].to(DEV) for n in ("q", "k", "v"))
+    oa_ref, la_ref = fa.forward(qa, ka, va, causal=True)
+    ob_ref, lb_ref = fa.forward(qb, kb, vb, causal=True)
+    fa.sync_status()
+    wsa, wsb = (torch.empty(256, dtype=torch.uint8, device=DEV) for _ in range(2))
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    sa.wait_stream(torch.cuda.current_stream())
+    sb.wait_stream(torch.cuda.current_stream())
+    oa, la = fa.forward(qa, ka, va, causal=True, workspace=wsa, stream=sa)
+    ob, lb = fa.forward(qb, kb, vb, causal=True, workspace=wsb, stream=sb)
+    sa.synchronize()
+    sb.synchronize()
+    fa.sync_status()
+    assert torch.equal(oa, oa_ref) and torch.equal(la, la_ref)
+    assert torch.equal(ob, ob_ref) and torch.equal(lb, lb_ref)
+
+
 def test_large_scores_dynamic_range():
     """Scores of magnitude ~100: the running max moves by far more than the
     rescale threshold, many times per row."""

@@ -350,6 +350,21 @@ def run_gpu(args, world, rank, local):
         "ms_per_launch": per[dom],
     }
 
+    # every kernel of the step against its own bound: the three tensor-core kernels
+    # in algorithmic TFLOP/s (the dQ kernel also in MMA work: its recomputed S and
+    # dP make it 1.5 f_fwd of products), prep in algorithmic GB/s against the
+    # measured copy bandwidth
+    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    prep_bytes = (4 * w.N * w.d + 12 * w.N) * w.B * w.H
+    kernels = {}
+    for name, flops, mma in (("fwd", f_fwd, f_fwd), ("bwd_dkdv", 2.0 * f_fwd, 2.0 * f_fwd),
+                             ("bwd_dq", 0.5 * f_fwd, 1.5 * f_fwd)):
+        t = flops / (per[name] / 1e3) / 1e12
+        kernels[name] = {"ms": per[name], "tflops": t, "frac_of_sustained": t / peak_sus,
+                         "mma_tflops": mma / (per[name] / 1e3) / 1e12}
+    gbs = prep_bytes / (per["bwd_prep"] / 1e3) / 1e9
+    kernels["bwd_prep"] = {"ms": per["bwd_prep"], "gbs": gbs, "frac_of_hbm": gbs / hbm}
+
     kname = roofline["kernel"]
     roofline["traffic"] = profiled_traffic(kname)
     if roofline["traffic"] is not None:
@@ -486,7 +501,7 @@ def run_gpu(args, world, rank, local):
         "data": "synthetic", "config": workload_config(w),
         "pct_of_bf16_peak": 100.0 * value / world / peak_burst,
         "peak_bf16_tflops": peak_burst, "peak_source": peak_src,
-        "kernel_ms": per, "roofline": roofline, "e2e": e2e,
+        "kernel_ms": per, "kernels": kernels, "roofline": roofline, "e2e": e2e,
         "gpu_launches": 4 * args.steps,
         "clocks": clk, "forward_gate": fwd_gate, "forward_gate_long": fwd_long, "fp8_forward": fp8,
     }

@@ -227,10 +227,10 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     if (warp == 0) {
         // ===================== loads =====================
         // Per item: fetch its index and publish it to the other roles; then the
-        // first query tile's Q and dO, K_j and V_j (their buffers hold the previous
-        // item's staged dK / dV until the store warp has read them), and the
-        // remaining query tiles.  Q and dO use rings indexed by the CTA's running
-        // tile count g, so one item's tiles follow the previous item's.
+        // first query tile's Q and dO, K_j and V_j (each buffer once the previous
+        // item's last S^T / dP^T has read it), and the remaining query tiles.  Q
+        // and dO use rings indexed by the CTA's running tile count g, so one
+        // item's tiles follow the previous item's.
         if (lane == 0) {
             tma_prefetch_desc(&tq);
             tma_prefetch_desc(&tk);

@@ -194,7 +194,7 @@ __device__ __forceinline__ void load_rows16(const uint16_t* src, int N, int row0
 
 // grid (tiles, BH, 2): Q (z = 0) and K (z = 1).
 template <int MODE>
-__global__ void __launch_bounds__(256) fa_fp8_quant_qk_kernel(const __grid_constant__ Fp8Args a) {
+__global__ void __launch_bounds__(256, 3) fa_fp8_quant_qk_kernel(const __grid_constant__ Fp8Args a) {
     __shared__ float red[8];
     const int tile = static_cast<int>(blockIdx.x);
     const int bh = static_cast<int>(blockIdx.y);
@@ -270,10 +270,11 @@ __global__ void __launch_bounds__(256) fa_fp8_quant_qk_kernel(const __grid_const
 }
 
 // grid (tiles, BH): V, written transposed ([BH, d, npad]) with each tile's keys
-// in P's order; the tile goes through shared memory for the transpose.
+// in P's order; the tile goes through shared memory for the transpose, kept as
+// the bf16 values it was read as (33 KB, so several CTAs share an SM).
 template <int MODE>
 __global__ void __launch_bounds__(256) fa_fp8_quant_v_kernel(const __grid_constant__ Fp8Args a) {
-    extern __shared__ float tl[];  // [128][129] fp32 tile (row stride 129 against bank conflicts)
+    extern __shared__ uint16_t tl[];  // [128][130] bf16 tile (row stride 65 words against bank conflicts)
     __shared__ float red[8];
     const int tile = static_cast<int>(blockIdx.x);
     const int bh = static_cast<int>(blockIdx.y);
@@ -290,7 +291,7 @@ __global__ void __launch_bounds__(256) fa_fp8_quant_v_kernel(const __grid_consta
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
             m = fmaxf(m, fabsf(x[p][e]));
-            if (MODE == 1) tl[(rl0 + 32 * p) * 129 + 16 * g + e] = x[p][e];
+            if (MODE == 1) tl[(rl0 + 32 * p) * 130 + 16 * g + e] = static_cast<uint16_t>(__float_as_uint(x[p][e]) >> 16);
         }
     const float amax_tile = cta_amax(m, red);  // (its barrier also orders the tile writes)
     if (MODE == 0) {
@@ -305,7 +306,8 @@ __global__ void __launch_bounds__(256) fa_fp8_quant_v_kernel(const __grid_consta
     for (int col = warp; col < kHD; col += 8) {
         float v[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) v[e] = tl[p_key_of_index(4 * lane + e) * 129 + col] * r;
+        for (int e = 0; e < 4; ++e)
+            v[e] = __uint_as_float(static_cast<uint32_t>(tl[p_key_of_index(4 * lane + e) * 130 + col]) << 16) * r;
         reinterpret_cast<uint32_t*>(dst + static_cast<size_t>(col) * npad)[lane] =
             e4m3x2(v[0], v[1]) | (e4m3x2(v[2], v[3]) << 16);
     }
@@ -789,7 +791,7 @@ fa_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
 }  // namespace
 
 cudaError_t launch_fp8_quant(const Fp8Args& a, cudaStream_t stream) {
-    const size_t smem_v = 128 * 129 * sizeof(float);
+    const size_t smem_v = 128 * 130 * sizeof(uint16_t);
     cudaError_t e = cudaFuncSetAttribute(fa_fp8_quant_v_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem_v));
     if (e != cudaSuccess) return e;

@@ -96,13 +96,13 @@ def test_stage_entry_points_match_fa_bwd():
     assert torch.equal(dq1, dq2) and torch.equal(dk1, dk2) and torch.equal(dv1, dv2)
 
 
-@pytest.mark.parametrize("N,d", [(128, 128), (256, 128), (128, 64), (256, 64)])
+@pytest.mark.parametrize("N,d", [(128, 128), (256, 128), (200, 128), (128, 64), (256, 64), (200, 64)])
 @pytest.mark.parametrize("causal", [False, True])
 def test_many_short_items_per_cta(N, d, causal):
-    """400 heads of one or two 128-row tiles: the persistent dK/dV and dQ kernels
-    (one CTA per SM) each run several short work items back to back, so item
-    hand-over, the rings that run on across items and the per-item barriers are
-    exercised many times per CTA."""
+    """400 heads of one or two 128-row tiles (N = 200: the second one ragged): the
+    persistent dK/dV and dQ kernels (one CTA per SM) each run several short work
+    items back to back, so item hand-over, the rings that run on across items
+    and the per-item barriers are exercised many times per CTA."""
     B, H = 2, 200
     scale = 1.0 / math.sqrt(d)
     inp = small_inputs(B, H, N, d, seed=3000 + N + d + causal)

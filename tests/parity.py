@@ -78,7 +78,8 @@ def bits(t):
 
 def with_guard(shape, dtype, device, guard=4096, fill=None):
     """A buffer of `shape` placed inside a larger allocation whose guard bands
-    before and after hold a known pattern; returns (view, checker)."""
+    before and after hold a known pattern; returns (view, check), where check()
+    asserts that the guard bands are unchanged."""
     n = int(np.prod(shape))
     big = torch.empty(n + 2 * guard, dtype=dtype, device=device)
     pattern = torch.full((guard,), -12345.0 if fill is None else fill, dtype=dtype, device=device)

@@ -118,7 +118,7 @@ PARITY_CASES = [
     (1, 2, 1000, False, False, False),
     (1, 1, 1357, True, True, True),
     (1, 2, 2048, True, True, False),
-    # more work items than SMs: each CTA of the persistent launch runs several
+    # more work items than SMs: several waves of CTAs, one item each
     (4, 100, 256, True, True, False),
     (2, 80, 384, False, True, False),  # the second Q tile of every second item is past N
 ]

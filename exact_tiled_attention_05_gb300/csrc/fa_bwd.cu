@@ -646,7 +646,8 @@ int grid_for(long long work_items, int per_block, int max_blocks) {
 
 cudaError_t launch_bwd_prep(int d, const BwdArgs& a, cudaStream_t stream) {
     const long long rows = static_cast<long long>(a.BH) * a.n_kblk * 128;
-    const int grid = grid_for(rows, 8 * (32 / (d / 8)) * 4, 152 * 8);  // 8 warps x 4 passes of 32/(d/8) rows
+    // 8 warps x 4 passes of 32/(d/8) rows per CTA, up to 8 CTAs per SM
+    const int grid = grid_for(rows, 8 * (32 / (d / 8)) * 4, 8 * (a.sms > 0 ? a.sms : 1));
     if (d == 64)
         fa_bwd_prep_kernel<64><<<grid, 256, 0, stream>>>(a);
     else

@@ -319,7 +319,8 @@ def quantize_fp8(q, k, v, signs=None, rotate=True, per_tensor=False, workspace=N
     B, H, N, d = _check_qkv(q, k, v)
     nbytes = fp8_workspace_bytes(B, H, N, d)
     if nbytes == 0:
-        raise ValueError("the FP8 forward supports head dimension 128 only")
+        raise ValueError("the FP8 forward takes head dimension 128, B*H <= 65535 and "
+                         "B*H*ceil(N/128)*128*128 < 2^31 only")
     if workspace is None:
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
     flags = (FA_FP8_ROTATE if rotate else 0) | (FA_FP8_PER_TENSOR if per_tensor else 0)

@@ -195,6 +195,8 @@ int fp8_shape(int B, int H, int N, int d) {
     if (d != 128) return kErrUnsupported;
     const int64_t rows = static_cast<int64_t>(B) * H * ((static_cast<int64_t>(N) + 127) / 128) * 128;
     if (rows * 128 >= (int64_t(1) << 31)) return kErrInvalidArg;
+    // the quantizers launch one CTA row per head on the grid's y dimension
+    if (static_cast<int64_t>(B) * H > 65535) return kErrUnsupported;
     return kOk;
 }
 

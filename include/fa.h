@@ -168,14 +168,16 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
 #define FA_FP8_ROTATE 1     /* rotate Q and K rows by diag(s) H / sqrt(128) */
 #define FA_FP8_PER_TENSOR 2 /* one scale per tensor (the pages' baseline) instead of per tile */
 
-/* Bytes of FP8 workspace for these sizes (0 for d != 128 or non-positive sizes). */
+/* Bytes of FP8 workspace for these sizes (0 for sizes the FP8 path does not
+ * take: d != 128, non-positive sizes, B*H > 65535, or B*H*128*ceil(N/128)*128
+ * >= 2^31). */
 size_t fa_fp8_workspace_size(int B, int H, int N, int d);
 
 /* Quantize q, k, v (bf16 [B,H,N,128]) into the workspace.  signs: host array
  * of 4 uint32 words, bit j (word j/32, bit j%32) set means s_j = -1; read
  * during the call, may be NULL when FA_FP8_ROTATE is not in flags.  flags: an
  * OR of FA_FP8_ROTATE and FA_FP8_PER_TENSOR.  Errors: FA_ERR_UNSUPPORTED for
- * d != 128, FA_ERR_WORKSPACE for a missing, misaligned or small workspace,
+ * d != 128 or B*H > 65535, FA_ERR_WORKSPACE for a missing, misaligned or small workspace,
  * FA_ERR_INVALID_ARG for unknown flags or a NULL signs with FA_FP8_ROTATE. */
 int fa_fp8_quantize(const void* q, const void* k, const void* v, int B, int H, int N, int d,
                     const unsigned int* signs, int flags, void* workspace,

@@ -52,6 +52,21 @@ def test_workspace_size(lib):
     assert fa.fa_bwd_workspace_size(0, 1, 1, 64) == 0
 
 
+def test_fp8_workspace_size_limits(lib):
+    """The FP8 path takes d = 128 only, at most 65535 heads (B*H) and fewer
+    than 2^31 code bytes per tensor; outside that the size is 0 and the calls
+    refuse the shape before any launch."""
+    assert fa.fa_fp8_workspace_size(1, 65535, 128, 128) > 0
+    assert fa.fa_fp8_workspace_size(1, 65536, 128, 128) == 0
+    assert fa.fa_fp8_workspace_size(256, 256, 1, 128) == 0
+    assert fa.fa_fp8_workspace_size(1, 1, 128, 64) == 0
+    assert fa.fa_fp8_workspace_size(1, 1, 1 << 24, 128) == 0  # 2^24 rows x 128 bytes = 2^31
+    assert fa.fa_fp8_workspace_size(1, 1, (1 << 24) - 128, 128) > 0
+    big = 1 << 40
+    assert fa.fa_fp8_quantize(FAKE, FAKE, FAKE, 1, 65536, 128, 128, None, 0, FAKE, big, None) == fa.FA_ERR_UNSUPPORTED
+    assert fa.fa_fwd_fp8(FAKE, big, FAKE, FAKE, 1, 65536, 128, 128, 0.1, 0, None) == fa.FA_ERR_UNSUPPORTED
+
+
 FAKE = 0x100000  # 16-byte aligned, never dereferenced: validation fails first
 
 

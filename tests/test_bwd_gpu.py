@@ -235,3 +235,33 @@ def test_entry_points_from_a_fresh_host_thread():
     for a_, b_ in zip(out["bwd"], g_ref):
         assert torch.equal(a_, b_)
     assert torch.equal(out["fp8"][0], o8_ref)
+
+
+def test_more_heads_than_a_grid_dimension():
+    """B*H = 100000 heads of N = 200 (past the 65535 limit of a launch grid's y
+    and z dimensions; every kernel here takes its work items on x or from a
+    counter).  61 seeded heads (a prime, so a wrong head index lands on another
+    pattern) tile all heads on the device: O, lse, dQ, dK and dV of every head
+    must equal its base head's bit for bit, and the base heads must match the
+    oracle."""
+    nb, N, d, B, H = 61, 200, 64, 4, 25000
+    scale = 1.0 / math.sqrt(d)
+    inp = small_inputs(1, nb, N, d, seed=4242)
+    reps = -(-(B * H) // nb)
+    big = {n: inp[n].to(DEV).repeat(1, reps, 1, 1)[:, :B * H].reshape(B, H, N, d).contiguous()
+           for n in ("q", "k", "v", "do")}
+    o, lse = fa.forward(big["q"], big["k"], big["v"], scale=scale, causal=True)
+    dq, dk, dv = fa.backward(big["q"], big["k"], big["v"], o, lse, big["do"], scale=scale, causal=True)
+    fa.sync_status()
+    del big
+    base = torch.arange(B * H, device=DEV) % nb
+    outs = {"o": o.reshape(B * H, N, d), "lse": lse.reshape(B * H, N), "dq": dq.reshape(B * H, N, d),
+            "dk": dk.reshape(B * H, N, d), "dv": dv.reshape(B * H, N, d)}
+    for name, t in outs.items():
+        assert torch.equal(t, t[:nb][base]), f"{name}: a head differs from its base head"
+    g = oracle.bwd(bits(inp["q"]), bits(inp["k"]), bits(inp["v"]), bits(inp["do"]), scale, True)
+    for name, ref in (("dq", g[0]), ("dk", g[1]), ("dv", g[2])):
+        check_grad(to_np(outs[name][:nb]), ref, f"{name}, 100000 heads")
+    err = np.abs(to_np(outs["o"][:nb]) - g[3])
+    assert err.max() <= 1e-2 and err.mean() <= 1e-3
+    assert np.abs(to_np(outs["lse"][:nb]) - g[4]).max() <= 1e-3

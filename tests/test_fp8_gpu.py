@@ -242,3 +242,32 @@ def test_rmse_outliers(kind):
           f"; per-tensor / (per-tile + rotation) = {r['tensor'] / r['tile+rotate']:.2f}")
     assert r["tile+rotate"] < r["tensor"]
     assert r["bf16"] < r["tile+rotate"]
+
+
+def test_fp8_largest_head_count():
+    """B*H = 65535, the most heads the FP8 path takes (the quantizers put heads
+    on the launch grid's y dimension).  61 seeded heads (a prime, so a wrong
+    head index lands on another pattern) tile all 65535 on the device: every
+    head's codes-based output must equal its base head's bit for bit, and the
+    base heads must meet the oracle's P-rounding bound."""
+    nb, N, B, H = 61, 128, 5, 13107
+    scale = 1.0 / math.sqrt(D)
+    inp = wl.outlier_inputs(1, nb, N, D, seed=77)
+    reps = -(-(B * H) // nb)
+    big = {n: inp[n].to(DEV).repeat(1, reps, 1, 1)[:, :B * H].reshape(B, H, N, D).contiguous()
+           for n in ("q", "k", "v")}
+    words = wl.sign_bits(78)
+    o, lse = fa.forward_fp8(big["q"], big["k"], big["v"], signs=words, causal=True)
+    fa.sync_status()
+    del big
+    o = o.reshape(B * H, N, D)
+    lse = lse.reshape(B * H, N)
+    base = torch.arange(B * H, device=DEV) % nb
+    assert torch.equal(o, o[:nb][base]) and torch.equal(lse, lse[:nb][base])
+    quant = oracle_quant(inp, words, True, False)
+    bound, o_ref, _ = ofp8.p_rounding_bound(quant, scale, True)
+    _, lse_ref = ofp8.attention_on_codes(quant, scale, True)
+    got = to_np(o[:nb])
+    slack = bf16_half_ulp(o_ref) + 1e-4 * np.abs(o_ref) + 1e-6
+    assert (np.abs(got - o_ref) - (bound + slack)).max() <= 0
+    check_lse(to_np(lse[:nb]), lse_ref, "fp8 lse, 65535 heads")

@@ -111,6 +111,27 @@ def test_fwd_32k_d128_sampled_rows():
     assert np.array_equal(o[:, 0, :], v0)
 
 
+@pytest.mark.parametrize("causal", [True, False])
+def test_fwd_one_million_keys_sampled_rows(causal):
+    """N = 2^20, d = 128, one head: 8192 query tiles, up to 8192 key tiles per
+    row block.  32 seeded rows (with 0, 1, 127, 128 and N-1) against the oracle."""
+    N, d = 1 << 20, 128
+    inp = wl.make_inputs(wl.WORKLOADS["fwd_32k_d128"], B=1, H=1, N=N, d=d, seed=90 + causal)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = run_fwd(inp, causal, scale)
+    rng = np.random.default_rng(91)
+    rows = np.unique(np.concatenate([[0, 1, 127, 128, N - 1], rng.choice(N, 27, replace=False)]))[None, :]
+    idx = torch.as_tensor(rows[0], device=o.device)
+    o_s = to_np(o.reshape(N, d)[idx])[None]
+    l_s = to_np(lse.reshape(N)[idx])[None]
+    o_ref, l_ref = oracle.fwd_rows(bits(inp["q"]), bits(inp["k"]), bits(inp["v"]), scale, causal, rows)
+    # rows 0 and 1 see one and two keys: the limits apply beyond the output rounding
+    check_o_beyond_rounding(o_s, o_ref, f"N=2^20 causal={causal}")
+    check_lse(l_s, l_ref, f"N=2^20 causal={causal}")
+    if causal:  # row 0 is exactly V[0]
+        assert np.array_equal(o_s[0, 0], inp["v"][0, 0, 0].double().numpy())
+
+
 # ---------------------------------------------------------------------------
 # ragged and degenerate shapes
 # ---------------------------------------------------------------------------

@@ -265,3 +265,24 @@ def test_more_heads_than_a_grid_dimension():
     err = np.abs(to_np(outs["o"][:nb]) - g[3])
     assert err.max() <= 1e-2 and err.mean() <= 1e-3
     assert np.abs(to_np(outs["lse"][:nb]) - g[4]).max() <= 1e-3
+
+
+@pytest.mark.parametrize("d,causal", [(128, True), (64, False)])
+def test_long_sequence_invariants(d, causal):
+    """N = 2^17 (1024 key and query tiles per head): too long for the oracle's
+    full gradients, so the identities that hold at any size are checked per
+    head and column: sum_j dK_j = 0 (each row of dS sums to zero) and
+    sum_j dV_j = sum_i dO_i (each row of P sums to one)."""
+    B, H, N = 1, 2, 1 << 17
+    scale = 1.0 / math.sqrt(d)
+    inp = small_inputs(B, H, N, d, seed=5000 + d)
+    _, _, dq, dk, dv = gpu_fwd_bwd(inp, causal, scale)
+    dq_n = to_np(dq).reshape(B * H, N, d)
+    dk_n = to_np(dk).reshape(B * H, N, d)
+    dv_n = to_np(dv).reshape(B * H, N, d)
+    assert np.isfinite(dq_n).all() and np.abs(dq_n).max() > 0
+    sk = np.abs(dk_n.sum(axis=1)) / np.maximum(np.abs(dk_n).sum(axis=1), 1e-30)
+    assert sk.max() <= 1e-2, f"sum_j dK_j not ~0: {sk.max()}"
+    do_n = inp["do"].double().numpy().reshape(B * H, N, d)
+    sv = np.abs(dv_n.sum(axis=1) - do_n.sum(axis=1)) / np.maximum(np.abs(dv_n).sum(axis=1), 1e-30)
+    assert sv.max() <= 1e-2, f"sum_j dV_j != sum_i dO_i: {sv.max()}"

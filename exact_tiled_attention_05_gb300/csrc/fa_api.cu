@@ -11,6 +11,17 @@
 #include "fa_internal.cuh"
 
 namespace fa {
+
+int check_shape(int B, int H, int N, int d, float scale, int causal) {
+    if (B < 1 || H < 1 || N < 1) return kErrInvalidArg;
+    if (causal != 0 && causal != 1) return kErrInvalidArg;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return kErrInvalidArg;
+    if (d != 64 && d != 128) return kErrUnsupported;
+    const int64_t total = static_cast<int64_t>(B) * H * N * d;
+    if (total >= (int64_t(1) << 31)) return kErrInvalidArg;
+    return kOk;
+}
+
 namespace {
 
 // Written by kernels that give up on a bounded wait; read and cleared by
@@ -146,16 +157,6 @@ int make_map_u8(CUtensorMap* map, const void* ptr, int x, int y, int z) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-int check_shape(int B, int H, int N, int d, float scale, int causal) {
-    if (B < 1 || H < 1 || N < 1) return kErrInvalidArg;
-    if (causal != 0 && causal != 1) return kErrInvalidArg;
-    if (!std::isfinite(scale) || !(scale > 0.f)) return kErrInvalidArg;
-    if (d != 64 && d != 128) return kErrUnsupported;
-    const int64_t total = static_cast<int64_t>(B) * H * N * d;
-    if (total >= (int64_t(1) << 31)) return kErrInvalidArg;
-    return kOk;
-}
 
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 

@@ -144,6 +144,11 @@ struct TensorMaps3 {
     CUtensorMap a, b, c;
 };
 
+// Shape and scalar checks shared by the forward and backward entry points:
+// B, H, N >= 1, causal 0 or 1, scale finite and > 0 (kErrInvalidArg); d 64 or
+// 128 (kErrUnsupported); B*H*N*d < 2^31 (kErrInvalidArg).  Defined in fa_api.cu.
+int check_shape(int B, int H, int N, int d, float scale, int causal);
+
 // Launchers (defined in the kernel translation units).  Return a cudaError_t.
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& to, const FwdArgs& args, cudaStream_t stream);

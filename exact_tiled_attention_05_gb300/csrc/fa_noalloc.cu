@@ -56,16 +56,25 @@ int scratch_for_current_device(void** out) {
 
 }  // namespace
 
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
 extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
                               const float* lse, const void* dout, void* dq, void* dk, void* dv,
                               int B, int H, int N, int d, float scale, int causal, void* stream) {
+    // The checks run in fa_bwd's order (pointers, shape, workspace, alignment),
+    // so a call gets the error fa_bwd would give with a large enough workspace;
+    // the fixed scratch stands in for that workspace.  Nothing touches the
+    // device before all of them pass.
     if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
-    if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
-    const size_t need = fa_bwd_workspace_size(B, H, N, d);
-    if (need == 0) return FA_ERR_INVALID_ARG;
-    if (need > kNoAllocScratchBytes) return FA_ERR_WORKSPACE;  // sizes beyond the fixed scratch
+    int rc = fa::check_shape(B, H, N, d, scale, causal);
+    if (rc != FA_OK) return rc;
+    if (fa_bwd_workspace_size(B, H, N, d) > kNoAllocScratchBytes) return FA_ERR_WORKSPACE;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) ||
+        !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
+        (reinterpret_cast<uintptr_t>(lse) & 3u))
+        return FA_ERR_MISALIGNED;
     void* scratch = nullptr;
-    const int rc = scratch_for_current_device(&scratch);
+    rc = scratch_for_current_device(&scratch);
     if (rc != FA_OK) return rc;
     return fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, causal, scratch,
                   kNoAllocScratchBytes, stream);

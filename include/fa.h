@@ -78,7 +78,13 @@ size_t fa_fwd_workspace_size(int B, int H, int N, int d);
 /* Bytes of device workspace fa_bwd needs for these sizes: two fp32 row
  * statistics, D = rowsum(dO * O) and -lse * log2(e), each [B*H, N rounded up to
  * a multiple of 128] and rounded up to 256 bytes, then 256 bytes for the work
- * counters of the dK/dV and dQ kernels (d does not change it). */
+ * counters of the dK/dV and dQ kernels (d does not change it).
+ * The statistics are those of the backward that rebuilds P from the saved
+ * logsumexp ("GPU 与 TPU：让硬件不再是黑魔法" (CS336 Lecture 5 notes) §11.5 (3):
+ * P = exp(S - L)): -L log2(e) makes the exponent of P one fused multiply-add,
+ * and D_i = sum_c dO[i,c] O[i,c] is the per-row term of the softmax Jacobian,
+ * dS = P * (dP - D), that the pages leave to the reader.  0 for non-positive
+ * sizes. */
 size_t fa_bwd_workspace_size(int B, int H, int N, int d);
 
 /* Backward pass.  Inputs q, k, v, o, lse (as written by fa_fwd) and dout
@@ -124,9 +130,12 @@ int fa_bwd_dq(const void* q, const void* k, const void* v, const float* lse,
  * allocation.  (The pages have no counterpart: this is a packaging choice of
  * this library.)  Same arguments, results and errors as fa_bwd, minus the workspace: the
  * scratch (fa_bwd_workspace_size bytes) lives in one fixed array of 64 MiB +
- * 256 bytes of library device memory, so nothing is allocated.  Sizes whose
- * workspace exceeds it (more than 2^23 rows B*H*N after rounding N up to a
- * multiple of 128) return FA_ERR_WORKSPACE before any launch.  The first call on a device looks up the array's device address with
+ * 256 bytes of library device memory, so nothing is allocated.  The checks run
+ * in fa_bwd's order: null pointers and bad sizes (FA_ERR_INVALID_ARG,
+ * FA_ERR_UNSUPPORTED) first, then the scratch limit: sizes whose workspace
+ * exceeds it (more than 2^23 rows B*H*N after rounding N up to a multiple of
+ * 128) return FA_ERR_WORKSPACE, then alignment (FA_ERR_MISALIGNED); all before
+ * any device call.  The first call on a device looks up the array's device address with
  * that device current; make that first call before any stream capture.  Every
  * call on a device shares the array: calls whose work overlaps on the GPU
  * (other streams, unordered host threads) race on it. */

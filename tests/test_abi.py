@@ -136,3 +136,27 @@ def test_missing_library_fails_loudly(tmp_path, monkeypatch):
     monkeypatch.setattr(fa, "_lib", None)
     with pytest.raises(RuntimeError):
         fa.load_library(str(tmp_path / "nope.so"))
+
+
+def test_noalloc_argument_checks_and_scratch_limit(lib):
+    """fa_bwd_noalloc checks its arguments in fa_bwd's order before touching the
+    device: bad pointers and shapes first, then its fixed scratch limit (2^23
+    padded rows, 64 MiB of row statistics + 256 bytes), then alignment.  A
+    misaligned pointer marks a size as accepted without any launch."""
+    def call(B, H, N, d, q=FAKE, scale=0.125, causal=1):
+        return fa.fa_bwd_noalloc(q, *([FAKE] * 8), B, H, N, d, scale, causal, None)
+
+    assert call(1, 1, 128, 64, q=None) == fa.FA_ERR_INVALID_ARG
+    assert call(1, 1, 0, 64) == fa.FA_ERR_INVALID_ARG
+    assert call(1, 1, 128, 64, causal=2) == fa.FA_ERR_INVALID_ARG
+    assert call(1, 1, 128, 64, scale=float("nan")) == fa.FA_ERR_INVALID_ARG
+    # the shape errors come first, even for sizes beyond the scratch
+    assert call(1, 64, 1 << 20, 96) == fa.FA_ERR_UNSUPPORTED
+    assert call(1 << 12, 1 << 12, 1 << 8, 128) == fa.FA_ERR_INVALID_ARG  # >= 2^31 elements
+    # the limit itself: B*H*ceil(N/128)*128 <= 2^23 rows
+    assert fa.fa_bwd_workspace_size(1, 64, 131072, 64) == (64 << 20) + 256
+    assert call(1, 64, 131072, 64, q=FAKE + 2) == fa.FA_ERR_MISALIGNED   # accepted size
+    assert call(1, 64, 131073, 64, q=FAKE + 2) == fa.FA_ERR_WORKSPACE    # one row over
+    assert call(1, 64, 131073, 64) == fa.FA_ERR_WORKSPACE
+    assert call(2, 32, 131072, 64, q=FAKE + 2) == fa.FA_ERR_MISALIGNED
+    assert call(1, 65, 131072, 64) == fa.FA_ERR_WORKSPACE

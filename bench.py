@@ -336,13 +336,15 @@ def run_gpu(args, world, rank, local):
     achieved = dom_flops / (per[dom] / 1e3) / 1e12 if dom_flops else None
     peak_sus = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
     peak_burst = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    peak, peak_kind = choose_peak(peaks, peak_src, elapsed_ms, clk)
     roofline = {
         "kernel": {"bwd_dkdv": "fa_bwd_dkdv_kernel<128>", "bwd_dq": "fa_bwd_dq_kernel<128>",
                    "fwd": "fa_fwd_kernel<128>"}.get(dom, dom),
-        "bound": "tensor", "achieved": achieved, "peak": peak_sus, "unit": "TFLOP/s",
-        "frac": achieved / peak_sus if achieved else None,
-        "peak_kind": f"bf16_tflops_sustained ({peak_src}), the kernel runs inside a long step loop",
-        "frac_of_burst_peak": achieved / peak_burst if achieved else None,
+        "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+        "frac": achieved / peak if achieved else None,
+        "peak_kind": peak_kind,
+        "frac_burst": achieved / peak_burst if achieved else None,
+        "frac_sustained": achieved / peak_sus if achieved else None,
         "traffic": None,
         "traffic_note": "dram__bytes_read.sum + dram__bytes_write.sum per launch from the committed "
                         "ncu capture under profiles/; null when the kernel changed since",
@@ -360,7 +362,8 @@ def run_gpu(args, world, rank, local):
     for name, flops, mma in (("fwd", f_fwd, f_fwd), ("bwd_dkdv", 2.0 * f_fwd, 2.0 * f_fwd),
                              ("bwd_dq", 0.5 * f_fwd, 1.5 * f_fwd)):
         t = flops / (per[name] / 1e3) / 1e12
-        kernels[name] = {"ms": per[name], "tflops": t, "frac_of_sustained": t / peak_sus,
+        kernels[name] = {"ms": per[name], "tflops": t, "frac": t / peak,
+                         "frac_burst": t / peak_burst, "frac_sustained": t / peak_sus,
                          "mma_tflops": mma / (per[name] / 1e3) / 1e12}
     gbs = prep_bytes / (per["bwd_prep"] / 1e3) / 1e9
     kernels["bwd_prep"] = {"ms": per["bwd_prep"], "gbs": gbs, "frac_of_hbm": gbs / hbm}
@@ -441,59 +444,59 @@ def run_gpu(args, world, rank, local):
            "gpu_launches": 4 * e2e_steps}
     del dev_in, dev_out
 
-    # ---------------- forward gate: N = 8192, d = 128, causal ----------------
+    # ---------------- sustained: the same step for at least 1.5 s ----------------
+    # (the timed region above is exactly --steps steps; this second region shows
+    # the rate once the GPU has settled at its power-capped clock)
+    sustained = sustained_rate(step, stream, dev, f_step, args.sustained_s, local)
+
+    # ---------------- forward-only workloads ----------------
+    # forward gate: N = 8192, d = 128, K x3, causal (inputs 201 MB > L2: no flush)
     wg = wl.WORKLOADS[FWD_GATE_WORKLOAD]
     gin = wl.make_inputs(wg, device=dev)
-    go = torch.empty_like(gin["q"])
-    gl = torch.empty(wg.B, wg.H, wg.N, dtype=torch.float32, device=dev)
-    for _ in range(3):
-        fa.forward(gin["q"], gin["k"], gin["v"], causal=True, out=go, lse=gl, workspace=fws)
-    reps = 50
-    fe = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
-    torch.cuda.synchronize(dev)
-    for a_, b_ in fe:
-        a_.record(stream)
-        fa.forward(gin["q"], gin["k"], gin["v"], causal=True, out=go, lse=gl, workspace=fws)
-        b_.record(stream)
-    torch.cuda.synchronize(dev)
+    fwd_gate = time_forward(fa, wg, gin, True, fws, stream, peak_burst, reps=50, flush=None,
+                            hbm_gbs=hbm)
+    fwd_gate["gate"] = ">= 60% of dense BF16 peak"
     check(fa.fa_sync_status(h), "forward gate")
-    fms = sorted(a_.elapsed_time(b_) for a_, b_ in fe)
-    f_gate = fwd_flops(wg) / (fms[reps // 2] / 1e3) / 1e12
-    fwd_gate = {"workload": f"fwd B={wg.B} H={wg.H} N={wg.N} d={wg.d} K x3 causal",
-                "ms_median": fms[reps // 2], "tflops": f_gate,
-                "pct_of_bf16_peak": 100.0 * f_gate / peak_burst,
-                "gate": ">= 60% of dense BF16 peak"}
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # 256 MB > the 129 MB L2
+    # B=4 H=16 N=2048 d=64, both masks (inputs 50 MB < L2: L2 flushed before each launch)
+    w64 = wl.WORKLOADS["fwd_2k_d64"]
+    in64 = wl.make_inputs(w64, device=dev)
+    fwd_d64 = {m: time_forward(fa, w64, in64, m == "causal", fws, stream, peak_burst, reps=50,
+                               flush=flush, hbm_gbs=hbm) for m in ("non_causal", "causal")}
+    # B=1 H=1 N=256 d=64, both masks: a single small launch (latency-bound)
+    w1 = wl.WORKLOADS["single_head_256"]
+    in1 = wl.make_inputs(w1, device=dev)
+    fwd_single = {m: time_forward(fa, w1, in1, m == "causal", fws, stream, peak_burst, reps=50,
+                                  flush=flush, hbm_gbs=hbm) for m in ("non_causal", "causal")}
+    del flush, in64, in1
+    check(fa.fa_sync_status(h), "forward d64")
 
     # ---------------- FP8 forward (quantize + FP8 attention), same workload ----------------
     fp8 = fp8_forward_timing(fa, wl, wg, gin, dev, stream, peak_burst)
     check(fa.fa_sync_status(h), "fp8 forward")
 
-    del gin, go, gl
+    del gin
 
     # ---------------- forward at N = 32768 (the long-context workload), causal ----------------
     wl32 = wl.WORKLOADS["fwd_32k_d128"]
     lin = wl.make_inputs(wl32, device=dev)
-    lo = torch.empty_like(lin["q"])
-    ll = torch.empty(wl32.B, wl32.H, wl32.N, dtype=torch.float32, device=dev)
-    for _ in range(3):
-        fa.forward(lin["q"], lin["k"], lin["v"], causal=True, out=lo, lse=ll, workspace=fws)
-    lreps = 10
-    le = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(lreps)]
-    torch.cuda.synchronize(dev)
-    for a_, b_ in le:
-        a_.record(stream)
-        fa.forward(lin["q"], lin["k"], lin["v"], causal=True, out=lo, lse=ll, workspace=fws)
-        b_.record(stream)
-    torch.cuda.synchronize(dev)
+    fwd_long = time_forward(fa, wl32, lin, True, fws, stream, peak_burst, reps=10, flush=None,
+                            hbm_gbs=hbm)
+    fwd_long["gate"] = ">= 60% of dense BF16 peak"
     check(fa.fa_sync_status(h), "forward 32k")
-    lms = sorted(a_.elapsed_time(b_) for a_, b_ in le)
-    f_long = fwd_flops(wl32) / (lms[lreps // 2] / 1e3) / 1e12
-    fwd_long = {"workload": f"fwd B={wl32.B} H={wl32.H} N={wl32.N} d={wl32.d} causal",
-                "ms_median": lms[lreps // 2], "tflops": f_long,
-                "pct_of_bf16_peak": 100.0 * f_long / peak_burst,
-                "gate": ">= 60% of dense BF16 peak"}
-    del lin, lo, ll
+    del lin
 
+    step_bytes = ((8 * N * d + 4 * N) + (12 * N * d + 8 * N) + (10 * N * d + 8 * N)
+                  + (4 * N * d + 12 * N)) * B * H
+    mhz = clk.get("sm_mhz") if clk else None
+    step_line = {"tflops": value / world, "frac": value / world / peak, "peak": peak,
+            "peak_kind": peak_kind, "frac_burst": value / world / peak_burst,
+            "frac_sustained": value / world / peak_sus,
+            "flops_per_step": f_step, "algorithmic_bytes_per_step": step_bytes,
+            "timed_region_ms": elapsed_ms,
+            "sm_mhz_median": mhz,
+            "ms_x_sm_mhz": ms_step * mhz if mhz else None,
+            "kcycles_per_step": ms_step * mhz if mhz else None}
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
@@ -501,14 +504,102 @@ def run_gpu(args, world, rank, local):
         "data": "synthetic", "config": workload_config(w),
         "pct_of_bf16_peak": 100.0 * value / world / peak_burst,
         "peak_bf16_tflops": peak_burst, "peak_source": peak_src,
+        "step": step_line, "sustained": sustained,
         "kernel_ms": per, "kernels": kernels, "roofline": roofline, "e2e": e2e,
         "gpu_launches": 4 * args.steps,
-        "clocks": clk, "forward_gate": fwd_gate, "forward_gate_long": fwd_long, "fp8_forward": fp8,
+        "clocks": clk, "forward_gate": fwd_gate, "forward_gate_long": fwd_long,
+        "forward_d64": fwd_d64, "forward_single_head": fwd_single, "fp8_forward": fp8,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = oracle_baseline(w, cpu_in)
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def choose_peak(peaks, peak_src, elapsed_ms, clk):
+    """Roofline denominator for kernels timed in the main region: the burst
+    BF16 peak (a short matmul loop) unless the timed region lasted seconds and
+    its median SM clock sits at or below the clock the sustained peak was
+    measured at (power-capped), then the sustained one."""
+    burst = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    sus = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    sus_mhz = (peaks.get("clocks_under_load") or {}).get("sm_mhz_median")
+    mhz = clk.get("sm_mhz") if clk else None
+    if elapsed_ms >= 2000.0 and mhz and sus_mhz and mhz <= 1.1 * sus_mhz:
+        return sus, (f"bf16_tflops_sustained ({peak_src}): timed region {elapsed_ms / 1e3:.1f} s at "
+                     f"a median {mhz:.0f} MHz, near the sustained peak's {sus_mhz:.0f} MHz")
+    return burst, (f"bf16_tflops burst ({peak_src}): timed region {elapsed_ms / 1e3:.2f} s at a "
+                   f"median {mhz} MHz" + (f" (sustained peak measured at {sus_mhz:.0f} MHz)"
+                                          if sus_mhz else ""))
+
+
+def sustained_rate(step, stream, dev, f_step, seconds, local):
+    """The fwd+bwd step repeated for at least `seconds` of device time: TFLOP/s
+    and the median SM clock sampled meanwhile."""
+    import torch
+    if seconds <= 0:
+        return None
+    probe = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    probe[0].record(stream)
+    for _ in range(10):
+        step()
+    probe[1].record(stream)
+    torch.cuda.synchronize(dev)
+    n = max(10, int(math.ceil(seconds * 1e3 / (probe[0].elapsed_time(probe[1]) / 10))))
+    clocks = ClockSampler(local)
+    clocks.start()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    a.record(stream)
+    for _ in range(n):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    ms = a.elapsed_time(b)
+    return {"steps": n, "seconds": ms / 1e3, "ms_per_step": ms / n,
+            "tflops": f_step * n / (ms / 1e3) / 1e12, "clocks": clk}
+
+
+def time_forward(fa, w, inp, causal, fws, stream, peak_burst, reps, flush, hbm_gbs=6779.0):
+    """Median CUDA-event time of `reps` forward launches (fa_fwd_ws) on one
+    workload; `flush` (a buffer larger than L2) is overwritten before every
+    launch, outside the timed events, when the inputs would fit in L2.  Returns
+    the line with its own roofline (tensor-bound: algorithmic FLOPs / time
+    against the burst BF16 peak; the launches are single and short)."""
+    import torch
+    o = torch.empty_like(inp["q"])
+    lse = torch.empty(w.B, w.H, w.N, dtype=torch.float32, device=inp["q"].device)
+    run = lambda: fa.forward(inp["q"], inp["k"], inp["v"], causal=causal, out=o, lse=lse,
+                             workspace=fws)
+    for _ in range(3):
+        run()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(reps)]
+    torch.cuda.synchronize()
+    for a_, b_ in ev:
+        if flush is not None:
+            flush.fill_(1)
+        a_.record(stream)
+        run()
+        b_.record(stream)
+    torch.cuda.synchronize()
+    ms = sorted(a_.elapsed_time(b_) for a_, b_ in ev)
+    med = ms[reps // 2]
+    flops = fwd_flops(w, causal)
+    tf = flops / (med / 1e3) / 1e12
+    alg_bytes = (8 * w.N * w.d + 4 * w.N) * w.B * w.H
+    mode = "causal" if causal else "non-causal"
+    extra = " K x3" if w.k_scale != 1.0 else ""
+    return {"workload": f"fwd B={w.B} H={w.H} N={w.N} d={w.d}{extra} {mode}",
+            "ms_median": med, "ms_min": ms[0], "tflops": tf,
+            "pct_of_bf16_peak": 100.0 * tf / peak_burst,
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": peak_burst, "unit": "TFLOP/s",
+                         "frac": tf / peak_burst, "flops_per_launch": flops,
+                         "algorithmic_bytes": alg_bytes,
+                         "hbm_floor_ms": alg_bytes / (hbm_gbs * 1e9) * 1e3},
+            "l2": "flushed before each launch (256 MB write)" if flush is not None
+                  else "inputs larger than L2"}
 
 
 def fp8_forward_timing(fa, wl, wg, gin, dev, stream, peak_bf16, reps=50):
@@ -603,6 +694,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sustained-s", type=float, default=1.5,
+                    help="seconds of back-to-back steps for the 'sustained' rate (0: skip)")
     ap.add_argument("--ref-budget-s", type=float, default=120.0,
                     help="--impl reference: seconds of oracle work for the whole run")
     ap.add_argument("--only", choices=("fwd", "fwd64", "bwd", "fp8"), default=None,

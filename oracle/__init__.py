@@ -13,6 +13,7 @@ from .oracle import (  # noqa: F401
     fwd_blockwise,
     fwd_rows,
     bwd,
+    bwd_rows,
     online_row,
     BF16,
     F64,

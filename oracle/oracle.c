@@ -461,3 +461,95 @@ int oracle_bwd(const void* q, const void* k, const void* v, const void* dout, in
     free(stats);
     return rc;
 }
+
+/* ------------------------------------------------------------------------- */
+/* backward for selected rows                                                */
+/* ------------------------------------------------------------------------- */
+
+typedef struct {
+    bwd_head_ctx* c;
+    const int64_t* rows; /* row indices of this head */
+} sel_ctx;
+
+/* Statistics of query row i only: m_i, l_i and D_i = dO_i . O_i. */
+static void stat_row_item(void* vctx, long item, double* scratch) {
+    sel_ctx* sc = (sel_ctx*)vctx;
+    bwd_head_ctx* c = sc->c;
+    long i = (long)sc->rows[item];
+    double* s = scratch;
+    double* p = scratch + c->N;
+    double* orow = scratch + 2 * c->N;
+    double m, l;
+    attend_row(c->h, i, c->N, c->d, c->scale, c->causal, s, p, orow, &m, &l);
+    c->m[i] = m;
+    c->l[i] = l;
+    c->D[i] = dot(c->h->dout + i * c->d, orow, c->d);
+}
+
+static void sel_row_item(void* vctx, long item, double* scratch) {
+    sel_ctx* sc = (sel_ctx*)vctx;
+    bwd_row_item(sc->c, (long)sc->rows[item], scratch);
+}
+
+static void sel_col_item(void* vctx, long item, double* scratch) {
+    sel_ctx* sc = (sel_ctx*)vctx;
+    bwd_col_item(sc->c, (long)sc->rows[item], scratch);
+}
+
+int oracle_bwd_rows(const void* q, const void* k, const void* v, const void* dout, int dtype,
+                    long BH, long N, long d, double scale, int causal,
+                    const int64_t* qrows, long nq, const int64_t* krows, long nk,
+                    double* dq_rows, double* dk_rows, double* dv_rows, int nthreads) {
+    if (check_common(q, k, v, dtype, BH, N, d) || !dout) return -1;
+    if (nq < 0 || nk < 0 || nq + nk < 1) return -1;
+    if (nq > 0 && (!qrows || !dq_rows)) return -1;
+    if (nk > 0 && (!krows || !dk_rows || !dv_rows)) return -1;
+    for (long t = 0; t < BH * nq; ++t) if (qrows[t] < 0 || qrows[t] >= N) return -1;
+    for (long t = 0; t < BH * nk; ++t) if (krows[t] < 0 || krows[t] >= N) return -1;
+    size_t nd = (size_t)N * (size_t)d;
+    double* stats = (double*)malloc((size_t)(3 * N) * sizeof(double));
+    double* full = (double*)malloc(3 * nd * sizeof(double)); /* dq, dk, dv of one head */
+    int64_t* need = (int64_t*)malloc((size_t)N * sizeof(int64_t));
+    if (!stats || !full || !need) { free(stats); free(full); free(need); return -2; }
+    int rc = 0;
+    for (long bh = 0; bh < BH && rc == 0; ++bh) {
+        head_t h;
+        rc = load_head(&h, q, k, v, dout, dtype, bh, N, d);
+        if (rc) break;
+        bwd_head_ctx c = { &h, N, d, scale, causal, stats, stats + N, stats + 2 * N,
+                           NULL, NULL, full, full + nd, full + 2 * nd };
+        /* the column pass of key row j reads the statistics of every query row
+         * that sees key j: all rows, or rows i >= j when causal */
+        long first = N;
+        for (long t = 0; t < nk; ++t) if (krows[bh * nk + t] < first) first = (long)krows[bh * nk + t];
+        if (nk > 0 && !causal) first = 0;
+        long n_need = 0;
+        for (long i = first; i < N; ++i) need[n_need++] = i;
+        if (n_need > 0) {
+            sel_ctx st = { &c, need };
+            rc = parallel_for(stat_row_item, &st, n_need, (size_t)(2 * N + d), nthreads);
+        }
+        if (rc == 0 && nq > 0) {
+            sel_ctx sq = { &c, qrows + bh * nq };
+            rc = parallel_for(sel_row_item, &sq, nq, (size_t)(2 * N + d), nthreads);
+            for (long t = 0; rc == 0 && t < nq; ++t)
+                memcpy(dq_rows + (bh * nq + t) * d, c.dq + qrows[bh * nq + t] * d,
+                       (size_t)d * sizeof(double));
+        }
+        if (rc == 0 && nk > 0) {
+            sel_ctx sk = { &c, krows + bh * nk };
+            rc = parallel_for(sel_col_item, &sk, nk, 0, nthreads);
+            for (long t = 0; rc == 0 && t < nk; ++t) {
+                memcpy(dk_rows + (bh * nk + t) * d, c.dk + krows[bh * nk + t] * d,
+                       (size_t)d * sizeof(double));
+                memcpy(dv_rows + (bh * nk + t) * d, c.dv + krows[bh * nk + t] * d,
+                       (size_t)d * sizeof(double));
+            }
+        }
+        free_head(&h);
+    }
+    free(stats);
+    free(full);
+    free(need);
+    return rc;
+}

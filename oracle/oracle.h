@@ -85,6 +85,18 @@ int oracle_bwd(const void* q, const void* k, const void* v, const void* dout, in
                double* dq, double* dk, double* dv,
                double* o_out, double* lse_out, int nthreads);
 
+/* Backward for selected rows of every head, by the same formulas as
+ * oracle_bwd: dq_rows [BH, nq, d] holds dQ of the query rows qrows [BH][nq];
+ * dk_rows, dv_rows [BH, nk, d] hold dK and dV of the key rows krows [BH][nk]
+ * (nq or nk may be 0, with NULL arrays).  dQ of row i needs only row i; dK and
+ * dV of key row j sum over every query row that sees key j, so the statistics
+ * m, l and D = dO . O of those rows (all rows, or rows i >= j when causal) are
+ * computed first.  The values equal oracle_bwd's for the same rows. */
+int oracle_bwd_rows(const void* q, const void* k, const void* v, const void* dout, int dtype,
+                    long BH, long N, long d, double scale, int causal,
+                    const int64_t* qrows, long nq, const int64_t* krows, long nk,
+                    double* dq_rows, double* dk_rows, double* dv_rows, int nthreads);
+
 /* Number of threads the oracle uses when asked for nthreads <= 0. */
 int oracle_default_threads(void);
 

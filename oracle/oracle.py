@@ -50,9 +50,11 @@ def _bind(path: str):
     lib.oracle_fwd_rows.argtypes = [vp, vp, vp, I, L, L, L, D, I, i64p, L, dp, dp, I]
     lib.oracle_fwd_blockwise.argtypes = [vp, vp, vp, I, L, L, L, D, I, L, L, dp, dp, I]
     lib.oracle_bwd.argtypes = [vp, vp, vp, vp, I, L, L, L, D, I, i64p, L, dp, dp, dp, dp, dp, I]
+    lib.oracle_bwd_rows.argtypes = [vp, vp, vp, vp, I, L, L, L, D, I, i64p, L, i64p, L,
+                                    dp, dp, dp, I]
     lib.oracle_default_threads.argtypes = []
     for f in ("oracle_online_row", "oracle_fwd", "oracle_fwd_rows",
-              "oracle_fwd_blockwise", "oracle_bwd", "oracle_default_threads"):
+              "oracle_fwd_blockwise", "oracle_bwd", "oracle_bwd_rows", "oracle_default_threads"):
         getattr(lib, f).restype = ctypes.c_int
     return lib
 
@@ -230,3 +232,30 @@ def bwd(q, k, v, dout, scale: float, causal: bool, heads=None, nthreads: int = 0
                             _dp(dq), _dp(dk), _dp(dv), _dp(o), _dp(lse), int(nthreads))
     _check(rc, "oracle_bwd")
     return dq, dk, dv, o, lse
+
+
+def bwd_rows(q, k, v, dout, scale: float, causal: bool, qrows=None, krows=None,
+             nthreads: int = 0):
+    """Backward for selected rows: qrows [BH, R] query rows whose dQ rows are
+    wanted, krows [BH, Rk] key rows whose dK and dV rows are wanted (either may
+    be None).  Returns (dq [BH,R,d] or None, dk [BH,Rk,d] or None, dv or None)."""
+    (q, k, v, dout), dt, BH, N, d = _prep(q, k, v, dout)
+
+    def rows_of(r):
+        if r is None:
+            return None, 0
+        r = np.ascontiguousarray(r, dtype=np.int64)
+        if r.ndim != 2 or r.shape[0] != BH:
+            raise ValueError("row lists must be [BH, R]")
+        return r, r.shape[1]
+
+    qr, nq = rows_of(qrows)
+    kr, nk = rows_of(krows)
+    dq = np.empty((BH, nq, d)) if nq else None
+    dk = np.empty((BH, nk, d)) if nk else None
+    dv = np.empty((BH, nk, d)) if nk else None
+    rc = _cur().oracle_bwd_rows(q.ctypes.data, k.ctypes.data, v.ctypes.data, dout.ctypes.data, dt,
+                                 BH, N, d, float(scale), int(bool(causal)), _i64p(qr), nq,
+                                 _i64p(kr), nk, _dp(dq), _dp(dk), _dp(dv), int(nthreads))
+    _check(rc, "oracle_bwd_rows")
+    return dq, dk, dv

@@ -75,22 +75,15 @@ def test_fwd_2k_d64_all_heads(causal):
     check_lse(to_np(lse).reshape(l_ref.shape), l_ref, "fwd 2k d64")
 
 
-def test_fwd_8k_d128_kx3_sampled_rows_and_full_heads():
+def test_fwd_8k_d128_kx3_all_heads():
+    """The forward-gate workload (B=2 H=16 N=8192 d=128, K x3, causal) in full:
+    every one of the 32 x 8192 rows of O and lse against the oracle."""
     w, inp, o, lse = workload_run("fwd_8k_d128_kx3", True)
-    qb, kb, vb = bits(inp["q"]), bits(inp["k"]), bits(inp["v"])
-    o = to_np(o).reshape(w.BH, w.N, w.d)
-    lse = to_np(lse).reshape(w.BH, w.N)
-    rows = wl.sampled_rows(w, count=256)
-    o_ref, l_ref = oracle.fwd_rows(qb, kb, vb, w.scale, True, rows)
-    o_s = np.take_along_axis(o, rows[:, :, None], axis=1)
-    l_s = np.take_along_axis(lse, rows, axis=1)
-    check_o(o_s, o_ref, "8k kx3 sampled rows")
-    check_lse(l_s, l_ref, "8k kx3 sampled rows")
-    heads = [0, w.BH - 1]
-    o_h, l_h = oracle.fwd(qb, kb, vb, w.scale, True, heads=heads)
-    check_o(o[heads], o_h, "8k kx3 full heads")
-    check_lse(lse[heads], l_h, "8k kx3 full heads")
-    print("8k kx3 full heads:", o_report(o[heads], o_h))
+    o_ref, l_ref = oracle.fwd(bits(inp["q"]), bits(inp["k"]), bits(inp["v"]), w.scale, True)
+    o = to_np(o).reshape(o_ref.shape)
+    check_o(o, o_ref, "8k kx3 all heads")
+    check_lse(to_np(lse).reshape(l_ref.shape), l_ref, "8k kx3 all heads")
+    print("8k kx3 all heads:", o_report(o, o_ref))
 
 
 def test_fwd_32k_d128_sampled_rows():

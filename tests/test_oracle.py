@@ -268,11 +268,52 @@ def pin_backward_invariants():
         assert np.max(np.abs(o - of)) < TIGHT and np.max(np.abs(lse - lf)) < TIGHT
 
 
+def pin_backward_rows_finite_differences():
+    """The sampled-row backward against central differences of sum(dO * O):
+    dQ of selected query rows, dK and dV of selected key rows (two heads, so a
+    statistic left over from the previous head would show)."""
+    q, k, v = _rng_inputs(19, BH=2, N=7, d=3, scale_k=1.5)
+    do = np.random.default_rng(20).standard_normal(q.shape)
+    scale = 0.8
+    qrows = np.array([[6, 0, 3], [2, 5, 1]], dtype=np.int64)
+    krows = np.array([[4, 1], [0, 6]], dtype=np.int64)
+    for causal in (False, True):
+        dq, dk, dv = oracle.bwd_rows(q, k, v, do, scale, causal, qrows=qrows, krows=krows)
+        for bh in range(2):
+            fq, fk, fv = _fd_grads(q[bh:bh + 1], k[bh:bh + 1], v[bh:bh + 1], do[bh:bh + 1],
+                                   scale, causal)
+            tol = 1e-7 * max(1.0, np.max(np.abs(fq)), np.max(np.abs(fk)), np.max(np.abs(fv)))
+            assert np.max(np.abs(dq[bh] - fq[0][qrows[bh]])) < tol
+            assert np.max(np.abs(dk[bh] - fk[0][krows[bh]])) < tol
+            assert np.max(np.abs(dv[bh] - fv[0][krows[bh]])) < tol
+
+
+def pin_backward_rows_equal_whole():
+    """The sampled-row backward gives the whole-head backward's values for the
+    same rows, bit for bit (the same row and column passes), with only query
+    rows, only key rows, or both asked for."""
+    q, k, v = _rng_inputs(23, BH=3, N=19, d=4, scale_k=2.0)
+    do = np.random.default_rng(24).standard_normal(q.shape)
+    rng = np.random.default_rng(25)
+    qrows = np.stack([rng.choice(19, 5, replace=False) for _ in range(3)])
+    krows = np.stack([rng.choice(19, 4, replace=False) for _ in range(3)])
+    for causal in (False, True):
+        dq, dk, dv, _, _ = oracle.bwd(q, k, v, do, 0.6, causal)
+        rq, rk, rv = oracle.bwd_rows(q, k, v, do, 0.6, causal, qrows=qrows, krows=krows)
+        oq, _, _ = oracle.bwd_rows(q, k, v, do, 0.6, causal, qrows=qrows)
+        _, ok, ov = oracle.bwd_rows(q, k, v, do, 0.6, causal, krows=krows)
+        for bh in range(3):
+            assert np.array_equal(rq[bh], dq[bh][qrows[bh]]) and np.array_equal(oq, rq)
+            assert np.array_equal(rk[bh], dk[bh][krows[bh]]) and np.array_equal(ok, rk)
+            assert np.array_equal(rv[bh], dv[bh][krows[bh]]) and np.array_equal(ov, rv)
+
+
 PINS = [
     pin_three_score_online, pin_three_score_attention, pin_six_score_online,
     pin_large_dynamic_range, pin_probability_rows, pin_two_keys_logistic,
     pin_causal_row0_and_zero_keys, pin_shift_and_affine_invariance, pin_permutations,
     pin_blockwise_equals_full, pin_backward_finite_differences, pin_backward_invariants,
+    pin_backward_rows_finite_differences, pin_backward_rows_equal_whole,
 ]
 
 
@@ -373,6 +414,12 @@ MUTATIONS = {
     "bwd_dv_uses_dS": ("dvj[cc] += Pij * doi[cc];", "dvj[cc] += dS * doi[cc];"),
     "bwd_D_from_v": ("double Di = dot(doi, orow, d);", "double Di = dot(doi, c->h->v + i * d, d);"),
     "bwd_dk_missing_scale": ("dkj[cc] += c->scale * dS * qi[cc];", "dkj[cc] += dS * qi[cc];"),
+    "bwd_rows_noncausal_stats_from_first_key": ("        if (nk > 0 && !causal) first = 0;\n", ""),
+    "bwd_rows_stats_one_row_late": ("for (long i = first; i < N; ++i) need[n_need++] = i;",
+                                    "for (long i = first + 1; i < N; ++i) need[n_need++] = i;"),
+    "bwd_rows_dq_copied_from_wrong_row": (
+        "memcpy(dq_rows + (bh * nq + t) * d, c.dq + qrows[bh * nq + t] * d,",
+        "memcpy(dq_rows + (bh * nq + t) * d, c.dq + qrows[bh * nq] * d,"),
 }
 
 

@@ -10,32 +10,41 @@ IO-Awareness Reshaped the Attention Kernel" §"FlashAttention-3", paragraph
   matrix M before quantizing, so (QM)(KM)^T = QK^T; M is a Hadamard transform
   with random sign flips, O(d log d) per row.
 
-Definitions here (fp64 unless stated):
+Definitions here, all in fp64 (the exact values of the method; nothing below
+follows any implementation's float32 operation order):
 
 * ``hadamard(d)``: the Sylvester matrix, H[i, j] = (-1)^popcount(i & j).
 * ``rotate(x, signs)``: (x * signs) @ H / sqrt(d), the orthogonal M = diag(s) H / sqrt(d).
 * ``e4m3_round(x)``: round-to-nearest-even onto the E4M3 grid (1 sign bit,
   4 exponent bits with bias 7, 3 mantissa bits, no infinities, largest finite
   448, subnormals in steps of 2^-9), values beyond 448 saturate to 448.
-* ``quantize_tiles``: per 128-row tile, scale = amax / 448 and codes =
-  e4m3_round(x * (448 / amax)); dequantized value = code * scale.  (The page
-  fixes one scale per tile; how a value becomes a code it leaves open: the
-  reading here maps the tile's amax onto E4M3's largest value 448.)
+* ``quantize_tiles``: per 128-row tile, A = max |x| over the tile, scale =
+  A / 448 and code = e4m3_round(x * 448 / A).  (The page fixes one scale per
+  tile; how a value becomes a code it leaves open: the reading here maps the
+  tile's amax onto E4M3's largest value 448.)
 
-``attention_on_codes`` is the attention the FP8 path approximates: the exact
-definition (``oracle.fwd``, fp64) applied to the dequantized codes.  The kernel
-also rounds the probabilities P to E4M3 before the P V product (the page says
-the path runs in FP8 but not how P is scaled); ``p_rounding_bound`` gives, per
-output element, the largest change that rounding can make under the reading
-the library documents (P * fold_j * 16 rounded to nearest E4M3, fp32 row sums,
-the largest weight of every tile corrected in the row sum), and is the parity
-tolerance of the GPU tests.
+A float32 implementation cannot reach these exact values: its rotation and its
+products round.  ``quantize_reference`` therefore also returns, per element, a
+band around the exact code-unit value x * 448 / A that holds every float32
+evaluation of the same definition whose rotation is a fast Walsh-Hadamard
+transform (log2(d) levels of a + b / a - b, then one multiplication by
+float32(1 / sqrt(d)); the page's O(d log d) rotation) and whose code value is
+formed with at most two more float32 roundings (a quotient or a reciprocal and
+a product).  ``codes_within_band`` accepts an implementation's code when it is
+the correctly rounded E4M3 of the exact value, or, only where the band
+straddles an E4M3 rounding boundary, either neighbour; it counts those cases.
+Scales are checked the same way (``scales_within_tolerance``).
 
-``rotate_f32`` restates the rotation as the butterfly network the kernel runs,
-in float32 with the same operation order, so that the kernel's FP8 codes can
-be compared bit for bit (both sides take the rounding decision in fp32).  It is
-pinned against ``rotate`` (fp64) and against ``scipy.linalg.hadamard`` by the
-tests.
+``attention_on_codes`` is exact attention (``oracle.fwd``, fp64) on the
+dequantized codes.  ``ideal_fp8_error`` is the error that exact E4M3 rounding
+of the block-quantized (and rotated) inputs causes against exact attention on
+the original inputs: the method's own accuracy, against which the FP8 path's
+error budget is stated.  ``p_rounding_bound`` is a diagnostic: per output
+element, the largest change that rounding the probabilities P to E4M3 can make
+under the reading the library documents (P * fold_j * 16 rounded to nearest
+E4M3, fp32 row sums, the largest weight of every tile corrected in the row
+sum); ``band_slack`` bounds the further change that the band cases' one-step
+code differences can make.
 """
 from __future__ import annotations
 
@@ -44,6 +53,7 @@ import math
 import numpy as np
 
 E4M3_MAX = 448.0
+U32 = 2.0 ** -24          # unit roundoff of float32 (round to nearest)
 
 
 def hadamard(d: int) -> np.ndarray:
@@ -69,37 +79,36 @@ def rotate(x: np.ndarray, signs: np.ndarray) -> np.ndarray:
     return (np.asarray(x, np.float64) * signs) @ hadamard(d) / math.sqrt(d)
 
 
-def rotate_f32(x: np.ndarray, signs: np.ndarray) -> np.ndarray:
-    """The same rotation as the kernel's float32 butterflies: element j of a
-    row is multiplied by s_j, then for h = 1, 2, 4, .., d/2 every pair
-    (a, b) = (v[i], v[i + h]) with i & h == 0 becomes (a + b, a - b), and the
-    result is multiplied by float32(1 / sqrt(d))."""
-    v = np.asarray(x, np.float32) * np.asarray(signs, np.float32)
-    d = v.shape[-1]
-    h = 1
-    while h < d:
-        v = v.reshape(v.shape[:-1] + (d // (2 * h), 2, h))
-        a = v[..., 0, :].copy()
-        b = v[..., 1, :].copy()
-        v[..., 0, :] = a + b
-        v[..., 1, :] = a - b
-        v = v.reshape(v.shape[:-3] + (d,))
-        h *= 2
-    return v * np.float32(1.0 / math.sqrt(d))
+def fwht_f32_error_bound(x: np.ndarray) -> np.ndarray:
+    """Per row of x [..., d] (values exact in float32), a bound on
+    |y32 - y| for every entry of the row, where y = rotate(x, s) and y32 is any
+    float32 fast Walsh-Hadamard transform of the sign-flipped row (log2(d)
+    levels of sums and differences, each rounding once) followed by one product
+    with float32(1 / sqrt(d)).  Each output is a sum of the d terms +-x_j
+    formed by an addition tree of depth L = log2(d), so its error is at most
+    gamma_L * sum_j |x_j| (gamma_L = L u / (1 - L u)); the constant and the
+    product add two more roundings: (L + 3) u sum_j |x_j| / sqrt(d) covers all
+    of it (u = 2^-24).  Returns [..., 1]."""
+    x = np.asarray(x, np.float64)
+    d = x.shape[-1]
+    L = int(round(math.log2(d)))
+    return (L + 3) * U32 * np.abs(x).sum(axis=-1, keepdims=True) / math.sqrt(d)
+
+
+def _binade(a: np.ndarray) -> np.ndarray:
+    """floor(log2 a) for a > 0, exactly, as int32 (frexp: a = m 2^e with m in
+    [0.5, 1)); -1 where a == 0."""
+    return np.frexp(a)[1] - np.int32(1)
 
 
 def e4m3_round(x: np.ndarray) -> np.ndarray:
     """Round to the nearest E4M3 value (ties to even), saturating at +-448."""
     x = np.asarray(x, np.float64)
     a = np.abs(x)
-    out = np.zeros_like(a)
-    nz = a > 0
-    e = np.where(nz, np.floor(np.log2(np.where(nz, a, 1.0))), 0.0)
-    e = np.clip(e, -6, 8)                 # below 2^-6: the subnormal step 2^-9
-    step = np.exp2(e - 3)
-    q = np.round(a / step) * step         # numpy rounds halves to even
-    out = np.where(nz, np.minimum(q, E4M3_MAX), 0.0)
-    return np.copysign(out, x)
+    e = np.clip(_binade(a), -6, 8)        # below 2^-6: the subnormal step 2^-9
+    step = np.ldexp(1.0, e - np.int32(3))
+    q = np.round(a / step) * step         # numpy rounds halves to even (exact: step is a power of 2)
+    return np.copysign(np.minimum(q, E4M3_MAX), x)
 
 
 def e4m3_decode(codes: np.ndarray) -> np.ndarray:
@@ -113,54 +122,50 @@ def e4m3_decode(codes: np.ndarray) -> np.ndarray:
 
 
 def e4m3_encode(x: np.ndarray) -> np.ndarray:
-    """E4M3 byte of each value (must already lie on the grid, |x| <= 448)."""
+    """E4M3 byte of each value (must already lie on the grid, |x| <= 448):
+    its magnitude in steps of 2^-9 below 2^-6 (exponent field 0), otherwise
+    exponent field e + 7 and mantissa (a / 2^e - 1) * 8."""
     x = np.asarray(x, np.float64)
     a = np.abs(x)
     sign = np.where(np.signbit(x), 0x80, 0)
-    code = np.zeros(a.shape, np.int64)
     sub = a < 2.0 ** -6
-    code = np.where(sub, np.round(a / 2.0 ** -9).astype(np.int64), code)
-    e = np.floor(np.log2(np.where(sub, 1.0, a))).astype(np.int64)
-    man = np.round((np.where(sub, 1.0, a) / np.exp2(e) - 1.0) * 8).astype(np.int64)
-    code = np.where(sub, code, ((e + 7) << 3) | man)
+    e = np.maximum(_binade(a), np.int32(-6))
+    man = np.round((np.ldexp(a, -e) - 1.0) * 8).astype(np.int32)
+    code = np.where(sub, np.round(a * 2.0 ** 9).astype(np.int32), ((e + 7) << 3) | man)
     return (code | sign).astype(np.uint8)
 
 
-def _scale_of(amax):
-    """fp32 scale amax / 448, or 1 where amax is 0."""
-    amax = np.asarray(amax, np.float32)
-    return np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
+def e4m3_step(x: np.ndarray) -> np.ndarray:
+    """Spacing of the E4M3 grid at |x| (the step up from |x|'s binade bottom)."""
+    e = np.clip(_binade(np.abs(np.asarray(x, np.float64))), -6, 8)
+    return np.ldexp(1.0, e - np.int32(3))
 
 
-def _factor_of(amax):
-    """fp32 factor 448 / amax that maps the tile onto E4M3's range, 1 where amax is 0."""
-    amax = np.asarray(amax, np.float32)
-    safe = np.where(amax > 0, amax, np.float32(1.0)).astype(np.float32)
-    return np.where(amax > 0, np.float32(E4M3_MAX) / safe, np.float32(1.0)).astype(np.float32)
+def _tile_amax(x: np.ndarray, tile: int, per_tensor: bool) -> np.ndarray:
+    """max |x| per 128-row tile [BH, T] (the whole tensor's max in every entry
+    when per_tensor)."""
+    BH, N, d = x.shape
+    nt = (N + tile - 1) // tile
+    if per_tensor:
+        return np.full((BH, nt), np.abs(x).max() if x.size else 0.0)
+    amax = np.zeros((BH, nt))
+    for t in range(nt):
+        amax[:, t] = np.abs(x[:, t * tile:(t + 1) * tile, :]).reshape(BH, -1).max(axis=1)
+    return amax
 
 
 def quantize_tiles(x: np.ndarray, tile: int = 128, per_tensor: bool = False):
-    """Per-tile scale and E4M3 codes of x [BH, N, d] in float32 arithmetic:
-    amax over the tile's rows (rows past N count as 0), scale = amax / 448 and
-    code = e4m3(x * (448 / amax)) (scale and factor 1 when the tile is all
-    zero), so that code * scale ~ x.  per_tensor: amax over the whole tensor
-    instead, the same scale for every tile.
-    Returns (codes uint8 [BH, N, d], scales float32 [BH, ceil(N/tile)])."""
-    x = np.asarray(x, np.float32)
+    """Per-tile scale and E4M3 codes of x [BH, N, d], in fp64: A = max |x| over
+    the tile's rows (the whole tensor when per_tensor), scale = A / 448 and
+    code = e4m3_round(x * 448 / A); scale 1 and code 0 for an all-zero tile.
+    Returns (codes uint8 [BH, N, d], scales float64 [BH, ceil(N/tile)])."""
+    x = np.asarray(x, np.float64)
     BH, N, d = x.shape
-    nt = (N + tile - 1) // tile
-    scales = np.ones((BH, nt), np.float32)
-    codes = np.zeros((BH, N, d), np.uint8)
-    whole = np.abs(x).max() if per_tensor else None
-    for t in range(nt):
-        blk = x[:, t * tile:(t + 1) * tile, :]
-        if per_tensor:
-            amax = np.full(BH, whole, np.float32)
-        else:
-            amax = np.abs(blk).reshape(BH, -1).max(axis=1).astype(np.float32)
-        scales[:, t] = _scale_of(amax)
-        y = (blk * _factor_of(amax)[:, None, None]).astype(np.float32)
-        codes[:, t * tile:(t + 1) * tile, :] = e4m3_encode(e4m3_round(y))
+    amax = _tile_amax(x, tile, per_tensor)
+    scales = np.where(amax > 0, amax / E4M3_MAX, 1.0)
+    rows = np.repeat(np.where(amax > 0, E4M3_MAX / np.where(amax > 0, amax, 1.0), 1.0),
+                     tile, axis=1)[:, :N]
+    codes = e4m3_encode(e4m3_round(x * rows[:, :, None]))
     return codes, scales
 
 
@@ -172,26 +177,88 @@ def dequantize_tiles(codes: np.ndarray, scales: np.ndarray, tile: int = 128) -> 
     return v * sc[:, :, None]
 
 
+def quantize_reference(x, signs=None, rotate_rows: bool = False, tile: int = 128,
+                       per_tensor: bool = False):
+    """The quantization of one input tensor x [BH, N, d] (values exact in
+    float32, such as bf16), exactly, plus the room a float32 evaluation has.
+
+    y = rotate(x, signs) when rotate_rows, else x; A = tile amax of y;
+    target t = y * 448 / A (code units, fp64); codes = e4m3_round(t).
+    With E the per-row rotation error bound (``fwht_f32_error_bound``; 0
+    without rotation) and E_A its largest value over the tile (|A32 - A| <=
+    E_A for the float32 amax A32), a float32 evaluation's code-unit value lies
+    within
+        band = (448 E + |t| E_A) / (A - E_A) + 3 u |t|
+    of t (3 u: the two roundings of 448 / A32 and the product, with room), and
+    its scale A32 / 448, rounded, within
+        scale_tol = (E_A + u (A + E_A)) / 448
+    of A / 448.  Returns a dict with codes, scales (fp64), target, band,
+    scale_tol ([BH, T])."""
+    x = np.asarray(x, np.float64)
+    BH, N, d = x.shape
+    y = rotate(x, signs) if rotate_rows else x
+    err = fwht_f32_error_bound(x) if rotate_rows else np.zeros((BH, N, 1))
+    codes, scales = quantize_tiles(y, tile, per_tensor)
+    amax = _tile_amax(y, tile, per_tensor)
+    if per_tensor:
+        e_a = np.full(amax.shape, err.max() if err.size else 0.0)
+    else:
+        e_a = _tile_amax(err, tile, False)
+    rows = lambda a: np.repeat(a, tile, axis=1)[:, :N, None]
+    A, EA = rows(amax), rows(e_a)
+    safe = np.where(A > 0, A, 1.0)
+    target = np.where(A > 0, y * E4M3_MAX / safe, 0.0)
+    band = np.where(A > 0, (E4M3_MAX * err + np.abs(target) * EA) / np.maximum(safe - EA, 1e-300)
+                    + 3 * U32 * np.abs(target), 0.0)
+    scale_tol = (e_a + U32 * (amax + e_a)) / E4M3_MAX
+    return {"codes": codes, "scales": scales, "target": target, "band": band,
+            "scale_tol": scale_tol, "amax": amax}
+
+
+def codes_within_band(got_codes: np.ndarray, ref: dict):
+    """Checks an implementation's E4M3 codes [BH, N, d] against
+    ``quantize_reference``: every code must decode to e4m3_round(target),
+    except where target - band and target + band round to different E4M3
+    values (the band straddles a rounding boundary); there either of the two
+    is accepted.  Returns (ok: bool, n_band: int, n_bad: int)."""
+    v = e4m3_decode(got_codes)
+    t, b = ref["target"], ref["band"]
+    exact = e4m3_round(t)
+    lo, hi = e4m3_round(t - b), e4m3_round(t + b)
+    ambiguous = lo != hi
+    ok_elem = np.where(ambiguous, (v == lo) | (v == hi), v == exact)
+    n_bad = int((~ok_elem).sum())
+    return n_bad == 0, int(ambiguous.sum()), n_bad
+
+
+def scales_within_tolerance(got_scales: np.ndarray, ref: dict):
+    """|scale32 - A / 448| <= scale_tol for every tile.  Returns (ok, worst ratio)."""
+    err = np.abs(np.asarray(got_scales, np.float64) - ref["scales"])
+    tol = np.where(ref["amax"] > 0, ref["scale_tol"], 0.0)
+    ratio = np.where(tol > 0, err / np.where(tol > 0, tol, 1.0), np.where(err > 0, np.inf, 0.0))
+    return bool(np.all(err <= tol)), float(ratio.max() if ratio.size else 0.0)
+
+
 def quantize_qkv(q, k, v, signs=None, rotate: bool = True, per_tensor: bool = False,
                  tile: int = 128):
-    """The quantization step for attention inputs [BH, N, d] (float32-exact
-    inputs such as bf16): Q and K rows rotated by diag(signs) H / sqrt(d)
-    (float32 butterflies) when ``rotate``, V never; then ``quantize_tiles``.
-    Returns {name: (codes, scales)} for q, k, v."""
-    q = np.asarray(q, np.float32)
-    k = np.asarray(k, np.float32)
-    v = np.asarray(v, np.float32)
-    if rotate:
-        q = rotate_f32(q, signs)
-        k = rotate_f32(k, signs)
-    return {"q": quantize_tiles(q, tile, per_tensor),
-            "k": quantize_tiles(k, tile, per_tensor),
-            "v": quantize_tiles(v, tile, per_tensor)}
+    """The quantization step for attention inputs [BH, N, d]: Q and K rows
+    rotated by diag(signs) H / sqrt(d) when ``rotate``, V never; each tensor
+    then quantized per tile (``quantize_reference``).  Returns {name: ref dict}
+    for q, k, v; ``codes_and_scales`` gives the plain (codes, scales) pairs."""
+    return {"q": quantize_reference(q, signs, rotate, tile, per_tensor),
+            "k": quantize_reference(k, signs, rotate, tile, per_tensor),
+            "v": quantize_reference(v, None, False, tile, per_tensor)}
+
+
+def codes_and_scales(quant):
+    """{name: (codes, scales)} of a ``quantize_qkv`` result."""
+    return {n: (r["codes"], r["scales"]) if isinstance(r, dict) else r for n, r in quant.items()}
 
 
 def dequantized_qkv(quant, tile: int = 128):
     """fp64 values code * scale of the three quantized tensors."""
-    return tuple(dequantize_tiles(*quant[n], tile=tile) for n in ("q", "k", "v"))
+    cs = codes_and_scales(quant)
+    return tuple(dequantize_tiles(*cs[n], tile=tile) for n in ("q", "k", "v"))
 
 
 def attention_on_codes(quant, scale: float, causal: bool, tile: int = 128):
@@ -203,6 +270,42 @@ def attention_on_codes(quant, scale: float, causal: bool, tile: int = 128):
                scale, causal)
 
 
+def attention_on_codes_rows(quant, scale: float, causal: bool, rows, tile: int = 128):
+    """``attention_on_codes`` for selected query rows [BH, R] only."""
+    from . import fwd_rows
+    qd, kd, vd = dequantized_qkv(quant, tile)
+    return fwd_rows(np.ascontiguousarray(qd), np.ascontiguousarray(kd), np.ascontiguousarray(vd),
+                    scale, causal, rows)
+
+
+def ideal_fp8_error(o_exact: np.ndarray, quant, scale: float, causal: bool, tile: int = 128,
+                    rows=None):
+    """The method's own FP8 error: exact attention on the exactly rounded codes
+    (``attention_on_codes``) against exact attention on the original inputs
+    (o_exact, [BH, N, d], or [BH, R, d] for the query rows ``rows``).
+    Returns (rmse, max |err|)."""
+    if rows is None:
+        o_codes, _ = attention_on_codes(quant, scale, causal, tile)
+    else:
+        o_codes, _ = attention_on_codes_rows(quant, scale, causal, rows, tile)
+    err = np.abs(o_codes - o_exact)
+    return float(np.sqrt((err ** 2).mean())), float(err.max())
+
+
+def fp8_budget(o_exact: np.ndarray, ideal):
+    """The FP8 forward's accuracy budget against exact attention on the
+    original inputs, from the method's own error ``ideal`` = (rmse, max) of
+    exact attention on exactly rounded codes: the FP8 path also rounds the
+    probabilities to E4M3 (3 mantissa bits, like V) and works in float32, so
+    it may double that error; the bf16 rounding of the output comes on top.
+        rmse <= 2 ideal_rmse + rms(half_ulp_bf16(O))
+        max  <= 2 ideal_max  + half_ulp_bf16(O)    (element by element)
+    Returns (rmse_budget, per-element max budget [same shape as o_exact])."""
+    a = np.maximum(np.abs(o_exact), np.finfo(np.float32).tiny)
+    half = np.ldexp(1.0, (np.floor(np.log2(a)) - 8).astype(np.int64))
+    return 2.0 * ideal[0] + float(np.sqrt((half ** 2).mean())), 2.0 * ideal[1] + half
+
+
 # E4M3 rounding of a probability y = P * c: |e4m3(y) - y| <= max(2^-4 y, 2^-10)
 # (half an ulp: 2^-4 relative in the normal range, half the subnormal step 2^-9
 # below 2^-6).
@@ -211,9 +314,14 @@ _HALF_SUB_STEP = 2.0 ** -10
 P_SCALE = 16.0
 
 
+def _vscales(quant):
+    r = quant["v"]
+    return (r["scales"] if isinstance(r, dict) else r[1]).astype(np.float64)
+
+
 def p_rounding_bound(quant, scale: float, causal: bool, tile: int = 128, rows=None):
-    """Per output element, the largest |O_fp8 - O_codes| that rounding P to
-    E4M3 can cause, O_codes = ``attention_on_codes``.
+    """Diagnostic: per output element, the largest |O_fp8 - O_codes| that
+    rounding P to E4M3 can cause, O_codes = ``attention_on_codes``.
 
     With p_k = exp(s_k - m) (m the row max), the weight of key k in tile j is
     rounded as y = p_k * c_j with c_j = 16 * sv_j / max_t sv_t (any running max
@@ -225,7 +333,7 @@ def p_rounding_bound(quant, scale: float, causal: bool, tile: int = 128, rows=No
     rows: optional int array [BH, R] of query rows to evaluate (all rows when
     None).  Returns (bound, o_codes, lse_codes), [BH, R, d], [BH, R, d], [BH, R]."""
     qd, kd, vd = dequantized_qkv(quant, tile)
-    sv = quant["v"][1].astype(np.float64)
+    sv = _vscales(quant)
     BH, N, d = qd.shape
     c = P_SCALE * sv / sv.max(axis=1, keepdims=True)            # [BH, T]
     key_tile = np.arange(N) // tile
@@ -258,3 +366,48 @@ def p_rounding_bound(quant, scale: float, causal: bool, tile: int = 128, rows=No
         lse[b] = m[:, 0] + np.log(l)
         bound[b] = (dp @ np.abs(vd[b]) + np.abs(o) * lc[:, None]) / (l - lc)[:, None]
     return bound, o_ref, lse
+
+
+def band_slack(quant, scale: float, causal: bool, tile: int = 128, rows=None):
+    """Diagnostic companion of ``p_rounding_bound``: where an element's band
+    straddles a rounding boundary, an implementation may hold the neighbouring
+    code, one E4M3 step (times the tile scale, widened by the scale tolerance)
+    away from the exact code.  Per query row i this moves each score by at most
+    ds_ij = scale (sum_c U_q[i,c] |k_jc| + |q_ic| U_k[j,c]) (U: those steps,
+    0 elsewhere; |q|, |k| widened by U), so the weights change by at most a
+    factor exp(+-2 max_j ds_ij), and O moves by at most
+    (exp(2 max_j ds_ij) - 1) max_j |v_j - O_i| + sum_j P_ij U_v[j] / (1 - ...).
+    Returns [BH, R, d] (all rows when rows is None)."""
+    qd, kd, vd = dequantized_qkv(quant, tile)
+    BH, N, d = qd.shape
+
+    def steps(name):
+        r = quant[name]
+        t, b = r["target"], r["band"]
+        amb = e4m3_round(t - b) != e4m3_round(t + b)
+        sc = np.repeat(r["scales"] + r["scale_tol"], tile, axis=1)[:, :N, None]
+        return np.where(amb, e4m3_step(np.abs(t) + b) * sc, 0.0)
+
+    uq, uk, uv = steps("q"), steps("k"), steps("v")
+    if rows is None:
+        rows = np.tile(np.arange(N), (BH, 1))
+    rows = np.asarray(rows, np.int64)
+    out = np.empty((BH, rows.shape[1], d))
+    for b in range(BH):
+        qa = np.abs(qd[b][rows[b]]) + uq[b][rows[b]]
+        ka = np.abs(kd[b]) + uk[b]
+        ds = scale * (uq[b][rows[b]] @ ka.T + qa @ uk[b].T)     # [R, N]
+        s = scale * (qd[b][rows[b]] @ kd[b].T)
+        vis = np.ones_like(s, dtype=bool)
+        if causal:
+            vis = np.arange(N)[None, :] <= rows[b][:, None]
+        s = np.where(vis, s, -np.inf)
+        p = np.exp(s - s.max(axis=1, keepdims=True))
+        p /= p.sum(axis=1, keepdims=True)
+        o = p @ vd[b]
+        dmax = np.where(vis, ds, 0.0).max(axis=1)                # [R]
+        growth = np.exp(2 * dmax) - 1.0
+        spread = np.stack([np.where(vis[i][:, None], np.abs(vd[b] - o[i][None, :]), 0.0).max(axis=0)
+                           for i in range(len(rows[b]))])       # [R, d]
+        out[b] = growth[:, None] * spread + (p @ uv[b]) * (1.0 + growth[:, None])
+    return out

@@ -113,8 +113,6 @@ def test_rotation_signs_come_first():
     s = np.where(np.arange(d) % 3 == 0, -1.0, 1.0)
     y = fp8.rotate(np.eye(d)[:1], s)[0]
     assert np.allclose(y, np.full(d, s[0] / math.sqrt(d)), rtol=0, atol=1e-15)
-    y32 = fp8.rotate_f32(np.eye(d)[:1], s)[0]
-    assert np.all(y32 == np.float32(s[0] / math.sqrt(d)))
 
 
 def test_rotation_is_orthogonal_and_keeps_scores():
@@ -127,16 +125,66 @@ def test_rotation_is_orthogonal_and_keeps_scores():
     assert np.abs(fp8.rotate(q, s) @ fp8.rotate(k, s).T - q @ k.T).max() < 1e-11
 
 
-def test_rotate_f32_matches_fp64_rotation():
+# Two float32 fast Walsh-Hadamard transforms written here, in the test, with
+# different operation orders (butterfly distance rising or falling; the
+# normalisation as a product with float32(1/sqrt(d)) or as a quotient by
+# float32(sqrt(d))), and two ways to form the code-unit value (x * (448/A) or
+# x / (A/448)).  The oracle's bands must hold every such evaluation.
+
+def fwht32(x, signs, rising=True, divide=False):
+    v = np.asarray(x, np.float32) * np.asarray(signs, np.float32)
+    d = v.shape[-1]
+    hs = [1 << i for i in range(int(math.log2(d)))]
+    for h in (hs if rising else hs[::-1]):
+        v = v.reshape(v.shape[:-1] + (d // (2 * h), 2, h))
+        a, b = v[..., 0, :].copy(), v[..., 1, :].copy()
+        v[..., 0, :] = a + b
+        v[..., 1, :] = a - b
+        v = v.reshape(v.shape[:-3] + (d,))
+    if divide:
+        return (v / np.float32(math.sqrt(d))).astype(np.float32)
+    return (v * np.float32(1.0 / math.sqrt(d))).astype(np.float32)
+
+
+def codes32(y, tile=128, per_tensor=False, quotient=False):
+    """float32 block quantization of float32 values y [BH, N, d]."""
+    y = np.asarray(y, np.float32)
+    BH, N, d = y.shape
+    nt = (N + tile - 1) // tile
+    codes = np.zeros(y.shape, np.uint8)
+    scales = np.ones((BH, nt), np.float32)
+    whole = np.abs(y).max()
+    for t in range(nt):
+        blk = y[:, t * tile:(t + 1) * tile]
+        amax = np.full(BH, whole, np.float32) if per_tensor else np.abs(blk).reshape(BH, -1).max(axis=1)
+        sc = np.where(amax > 0, amax / np.float32(448.0), np.float32(1.0)).astype(np.float32)
+        scales[:, t] = sc
+        if quotient:
+            tv = (blk / sc[:, None, None]).astype(np.float32)
+        else:
+            f = np.where(amax > 0, np.float32(448.0) / np.where(amax > 0, amax, 1), 1).astype(np.float32)
+            tv = (blk * f[:, None, None]).astype(np.float32)
+        codes[:, t * tile:(t + 1) * tile] = fp8.e4m3_encode(fp8.e4m3_round(tv))
+    return codes, scales
+
+
+@pytest.mark.parametrize("rising,divide", [(True, False), (False, True)])
+def test_fwht_error_bound_holds(rising, divide):
+    """Every entry of a float32 FWHT lies within fwht_f32_error_bound of the
+    fp64 rotation, for either butterfly order and normalisation, on inputs
+    with large outliers; the bound is not vacuous (the worst entry uses a
+    visible part of it)."""
     r = np.random.default_rng(2)
     d = 128
     s = np.where(r.random(d) < 0.5, -1.0, 1.0)
-    x = (r.standard_normal((200, d)) * 3).astype(np.float32)
+    x = (r.standard_normal((400, d)) * 3).astype(np.float32)
+    x[r.random(x.shape) < 0.01] *= 40
     y64 = fp8.rotate(x.astype(np.float64), s)
-    y32 = fp8.rotate_f32(x, s).astype(np.float64)
-    # seven butterfly levels and one scaling, each rounding to fp32
-    tol = 8 * 2.0 ** -24 * np.abs(x).sum(axis=1, keepdims=True) / math.sqrt(d)
-    assert np.all(np.abs(y32 - y64) <= tol)
+    y32 = fwht32(x, s, rising, divide).astype(np.float64)
+    tol = fp8.fwht_f32_error_bound(x)
+    ratio = np.abs(y32 - y64) / tol
+    assert ratio.max() <= 1.0
+    assert ratio.max() > 0.02
 
 
 def test_spike_spreads_evenly():
@@ -183,22 +231,29 @@ def test_tile_max_maps_to_448():
     codes, scales = fp8.quantize_tiles(x)
     for b in range(2):
         for t in range(3):
-            blk = x[b, 128 * t:128 * (t + 1)]
+            blk = x[b, 128 * t:128 * (t + 1)].astype(np.float64)
             i = np.unravel_index(np.abs(blk).argmax(), blk.shape)
             assert fp8.e4m3_decode(codes[b, 128 * t:128 * (t + 1)][i]) == math.copysign(448.0, blk[i])
-            assert scales[b, t] == np.float32(np.abs(blk).max()) / np.float32(448.0)
+            assert scales[b, t] == np.abs(blk).max() / 448.0
 
 
 def test_quantization_error_is_half_ulp():
+    """|code * scale - x| is at most half an E4M3 step of x / scale (2^-4
+    relative in the normal range, 2^-10 below 2^-6), up to the fp64 rounding
+    of the two products."""
     r = np.random.default_rng(5)
-    x = (r.standard_normal((1, 256, 32)) * 4).astype(np.float32)
+    x = (r.standard_normal((1, 256, 32)) * 4).astype(np.float32).astype(np.float64)
+    x[0, 3, :8] = np.ldexp(1.0, -np.arange(8) - 4) * x[0, 3, :8]   # tiny values: subnormal codes
     codes, scales = fp8.quantize_tiles(x)
-    deq = fp8.dequantize_tiles(codes, scales)
-    y = x.astype(np.float64) / np.repeat(scales.astype(np.float64), 128, axis=1)[:, :, None]
-    # (codes are taken from x * (448 / amax) in fp32, y up to two fp32 roundings)
+    sc = np.repeat(scales, 128, axis=1)[:, :, None]
+    y = x / sc
     bound = np.maximum(2.0 ** -4 * np.abs(y), 2.0 ** -10)   # in code units
-    err = np.abs(deq - x) / np.repeat(scales.astype(np.float64), 128, axis=1)[:, :, None]
-    assert np.all(err <= bound * (1 + 1e-6) + 4 * 2.0 ** -24 * np.abs(y))
+    err = np.abs(fp8.dequantize_tiles(codes, scales) - x) / sc
+    assert np.all(err <= bound * (1 + 1e-12))
+    # exactly half a grid step at most, and some values sit almost that far
+    half_step = fp8.e4m3_step(y) / 2
+    assert np.all(err <= half_step * (1 + 1e-12))
+    assert (err / half_step).max() > 0.99
 
 
 def test_tiles_are_independent_and_per_tensor_is_global():
@@ -209,9 +264,9 @@ def test_tiles_are_independent_and_per_tensor_is_global():
     cx, sx = fp8.quantize_tiles(x)
     cy, sy = fp8.quantize_tiles(y)
     assert np.array_equal(cx[:, 128:], cy[:, 128:]) and sx[0, 1] == sy[0, 1]
-    assert sy[0, 0] == np.float32(1000.0) / np.float32(448.0)
+    assert sy[0, 0] == 1000.0 / 448.0
     ct, st = fp8.quantize_tiles(y, per_tensor=True)
-    assert np.all(st == np.float32(1000.0) / np.float32(448.0))
+    assert np.all(st == 1000.0 / 448.0)
     assert not np.array_equal(ct[:, 128:], cy[:, 128:])
 
 
@@ -234,7 +289,7 @@ def test_attention_on_grid_values_is_lossless():
         x[n][:, 128, 0] = 448.0
     quant = fp8.quantize_qkv(x["q"], x["k"], x["v"], rotate=False)
     for n in "qkv":
-        assert np.all(quant[n][1] == 1.0)
+        assert np.all(quant[n]["scales"] == 1.0)
     o, lse = fp8.attention_on_codes(quant, 0.01, True)
     o_ref, lse_ref = oracle.fwd(x["q"], x["k"], x["v"], 0.01, True)
     assert np.array_equal(o, o_ref) and np.array_equal(lse, lse_ref)
@@ -259,7 +314,7 @@ def emulate_p_rounding(quant, scale, causal, tile=128):
     """P rounded as the bound describes (fp64 p against the row max, y = p c_j
     rounded to E4M3, the largest weight of each tile corrected in the row sum)."""
     qd, kd, vd = fp8.dequantized_qkv(quant, tile)
-    sv = quant["v"][1].astype(np.float64)
+    sv = quant["v"]["scales"].astype(np.float64)
     c = fp8.P_SCALE * sv / sv.max(axis=1, keepdims=True)
     BH, N, d = qd.shape
     jt = np.arange(N) // tile
@@ -307,6 +362,152 @@ def test_p_rounding_bound_holds(N, causal, vscale):
 
 
 # ---------------------------------------------------------------------------
+# the float32 bands of the codes and scales
+# ---------------------------------------------------------------------------
+
+def band_inputs(seed, BH=2, N=300, d=128):
+    """Random rows with outliers and a row of tiny values, plus, in every
+    128-row tile, 40 rows whose ROTATED values sit on E4M3 rounding midpoints
+    (with the tile's amax held at 448 so that code units are values): drawn
+    as midpoints, rotated back, rounded to float32.  Those rows' exact targets
+    lie within about one float32 rounding of a midpoint, so the code depends
+    on the float32 rotation's own error."""
+    r = np.random.default_rng(seed)
+    x = (r.standard_normal((BH, N, d)) * 2).astype(np.float32)
+    x[r.random(x.shape) < 0.002] *= 30                       # outliers
+    x[:, 5, :] *= np.float32(2.0 ** -12)                     # a row of tiny values (subnormal codes)
+    s = np.where(r.random(d) < 0.5, -1.0, 1.0)
+    grid = fp8.e4m3_decode(np.arange(0x38, 0x7E, dtype=np.uint8))   # 1 .. 416
+    mids = (grid[:-1] + grid[1:]) / 2
+    for t0 in range(0, N, 128):
+        rows = min(40, N - t0 - 10)
+        if rows <= 0:
+            continue
+        y = r.choice(mids, (BH, rows, d)) * np.where(r.random((BH, rows, d)) < 0.5, -1, 1)
+        y[:, 0, 0] = 448.0                                    # holds the amax at 448 (exactly)
+        m = fp8.rotate(np.eye(d), s)                          # rows of M
+        x[:, t0 + 10:t0 + 10 + rows, :] = (y @ m.T).astype(np.float32)
+    return x, s
+
+
+@pytest.mark.parametrize("rising,divide,quotient,per_tensor", [
+    (True, False, False, False), (False, True, True, False), (True, True, False, True),
+    (False, False, True, True)])
+def test_float32_quantizers_fall_within_the_bands(rising, divide, quotient, per_tensor):
+    """Four float32 quantizers with different operation orders (written in this
+    test): every code within codes_within_band, every scale within
+    scales_within_tolerance; some codes need the band (they differ from the
+    exact rounding), so the band is doing work."""
+    x, s = band_inputs(10 + rising + 2 * divide)
+    ref = fp8.quantize_reference(x, s, True, per_tensor=per_tensor)
+    c32, s32 = codes32(fwht32(x, s, rising, divide), per_tensor=per_tensor, quotient=quotient)
+    ok, n_band, n_bad = fp8.codes_within_band(c32, ref)
+    assert ok, f"{n_bad} codes outside the band"
+    differ = fp8.e4m3_decode(c32) != fp8.e4m3_round(ref["target"])
+    assert differ.sum() > 0 and n_band >= differ.sum()
+    ok_s, worst = fp8.scales_within_tolerance(s32, ref)
+    assert ok_s, f"scale error {worst:.2f} x the tolerance"
+    # without the rotation the band is a few float32 roundings of |t| wide
+    ref_v = fp8.quantize_reference(x, None, False, per_tensor=per_tensor)
+    cv, sv = codes32(x, per_tensor=per_tensor, quotient=quotient)
+    assert fp8.codes_within_band(cv, ref_v)[0]
+    assert fp8.scales_within_tolerance(sv, ref_v)[0]
+
+
+def test_band_rejects_a_code_one_step_off():
+    """A code one E4M3 step from the exact rounding where the band does not
+    straddle a boundary is rejected; so is a scale off by more than its
+    tolerance."""
+    x, s = band_inputs(20)
+    ref = fp8.quantize_reference(x, s, True)
+    t, b = ref["target"], ref["band"]
+    clear = (fp8.e4m3_round(t - b) == fp8.e4m3_round(t + b)) & (np.abs(t) > 1) & (np.abs(t) < 400)
+    idx = np.argwhere(clear)[7]
+    bad = ref["codes"].copy()
+    bad[tuple(idx)] += 1                                      # next code up in magnitude
+    assert fp8.codes_within_band(ref["codes"], ref)[0]
+    ok, _, n_bad = fp8.codes_within_band(bad, ref)
+    assert not ok and n_bad == 1
+    sc = ref["scales"].copy()
+    sc[0, 0] += 3 * ref["scale_tol"][0, 0]
+    assert not fp8.scales_within_tolerance(sc, ref)[0]
+
+
+def test_band_accepts_both_neighbours_at_a_tie():
+    """A value whose code-unit target is exactly a rounding midpoint (1.0625,
+    between 1 and 1.125): with a non-zero band both neighbours are accepted;
+    everywhere else only the exact rounding."""
+    x = np.zeros((1, 128, 4))
+    x[0, 0, 0] = 448.0                                         # amax = 448: code units = values
+    x[0, 1, 0] = 1.0625
+    x[0, 2, 0] = 1.03
+    ref = fp8.quantize_reference(x, None, False)
+    assert ref["target"][0, 1, 0] == 1.0625 and ref["band"][0, 1, 0] > 0
+    for v in (1.0, 1.125):
+        c = ref["codes"].copy()
+        c[0, 1, 0] = fp8.e4m3_encode(np.array([v]))[0]
+        assert fp8.codes_within_band(c, ref)[0]
+    c = ref["codes"].copy()
+    c[0, 2, 0] = fp8.e4m3_encode(np.array([1.125]))[0]        # 1.03 rounds to 1 only
+    assert not fp8.codes_within_band(c, ref)[0]
+
+
+def test_band_slack_covers_neighbour_codes():
+    """Flipping every straddling code of Q, K and V to its other neighbour
+    changes attention on the codes by no more than band_slack."""
+    r = np.random.default_rng(30)
+    BH, N, d = 1, 200, 128
+    q, k, v = ((r.standard_normal((BH, N, d)) * 2).astype(np.float32) for _ in range(3))
+    for t in (q, k):
+        t[r.random(t.shape) < 0.003] *= 30
+    s = np.where(r.random(d) < 0.5, -1.0, 1.0)
+    quant = fp8.quantize_qkv(q, k, v, s)
+    flipped = {}
+    n_flip = 0
+    for n in "qkv":
+        ref = quant[n]
+        t, b = ref["target"], ref["band"]
+        lo, hi = fp8.e4m3_round(t - b), fp8.e4m3_round(t + b)
+        exact = fp8.e4m3_round(t)
+        other = np.where(exact == lo, hi, lo)
+        amb = lo != hi
+        n_flip += int(amb.sum())
+        flipped[n] = dict(ref, codes=np.where(amb, fp8.e4m3_encode(other), ref["codes"]).astype(np.uint8))
+    assert n_flip > 0
+    o0, _ = fp8.attention_on_codes(quant, 0.09, True)
+    o1, _ = fp8.attention_on_codes(flipped, 0.09, True)
+    slack = fp8.band_slack(quant, 0.09, True)
+    assert np.all(np.abs(o1 - o0) <= slack * (1 + 1e-9) + 1e-15)
+    assert (np.abs(o1 - o0)).max() > 0
+
+
+def test_budget_of_exact_codes_is_met_by_exact_codes():
+    """The error budget against exact attention, fed the method's own ideal
+    error, holds for attention on the exactly rounded codes (by a factor of
+    two) and fails for codes of a coarser format (one mantissa bit fewer)."""
+    r = np.random.default_rng(31)
+    BH, N, d = 2, 256, 128
+    q, k, v = ((r.standard_normal((BH, N, d))).astype(np.float32) for _ in range(3))
+    s = np.where(r.random(d) < 0.5, -1.0, 1.0)
+    o_ex, _ = oracle.fwd(q.astype(np.float64), k.astype(np.float64), v.astype(np.float64),
+                         d ** -0.5, True)
+    quant = fp8.quantize_qkv(q, k, v, s)
+    ideal = fp8.ideal_fp8_error(o_ex, quant, d ** -0.5, True)
+    rmse_b, max_b = fp8.fp8_budget(o_ex, ideal)
+    o_c, _ = fp8.attention_on_codes(quant, d ** -0.5, True)
+    err = np.abs(o_c - o_ex)
+    assert np.sqrt((err ** 2).mean()) <= rmse_b / 2 + 1e-15 and np.all(err <= max_b)
+    # codes with two mantissa bits: the same inputs miss the budget
+    coarse = {}
+    for n in "qkv":
+        vals = fp8.e4m3_decode(quant[n]["codes"])
+        step = fp8.e4m3_step(vals) * 2
+        coarse[n] = dict(quant[n], codes=fp8.e4m3_encode(np.clip(np.round(vals / step) * step, -448, 448)))
+    o_2, _ = fp8.attention_on_codes(coarse, d ** -0.5, True)
+    assert np.sqrt(((o_2 - o_ex) ** 2).mean()) > rmse_b
+
+
+# ---------------------------------------------------------------------------
 # planted mistakes: a wrong oracle must fail a pin
 # ---------------------------------------------------------------------------
 
@@ -337,3 +538,12 @@ def test_planted_wrong_scale_is_caught():
     bad_scale = amax / np.float32(240.0)                 # E4M3's other maximum convention
     code = fp8.e4m3_round(np.array([amax / bad_scale]))[0]
     assert code != 448.0                                 # the max-to-448 pin rejects it
+
+
+def test_planted_narrow_band_is_caught(monkeypatch):
+    """A band without the rotation's error term (a plausible slip in the error
+    analysis: only the roundings of the code-unit product counted) leaves
+    float32 codes outside it: the float32 quantizer pin catches it."""
+    monkeypatch.setattr(fp8, "fwht_f32_error_bound", lambda x: np.zeros(x.shape[:-1] + (1,)))
+    with pytest.raises(AssertionError):
+        test_float32_quantizers_fall_within_the_bands(True, False, False, False)

@@ -202,7 +202,8 @@ def forward(q, k, v, scale=None, causal=False, out=None, lse=None, workspace=Non
     Returns (o bf16 [B,H,N,d], lse fp32 [B,H,N]).  Runs fa_fwd_ws: `workspace`
     (uint8 CUDA tensor of fa_fwd_workspace_size bytes) holds the kernel's work
     counter, and one is allocated when none is given.  workspace=False runs
-    fa_fwd instead (no workspace, one CTA per work item, same results)."""
+    fa_fwd instead (no workspace: a static schedule of the same items, same
+    results)."""
     torch = _torch()
     B, H, N, d = _check_qkv(q, k, v)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)

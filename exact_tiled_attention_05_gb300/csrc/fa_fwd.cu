@@ -36,6 +36,15 @@
 //
 // Causal: key tiles entirely in the future of a Q tile are never loaded or
 // multiplied; the diagonal tile and a ragged last tile are masked per element.
+#include <functional>
+#include <map>
+#include <memory>
+#include <mutex>
+#include <queue>
+#include <tuple>
+#include <utility>
+#include <vector>
+
 #include "fa_internal.cuh"
 #include "ptx.cuh"
 
@@ -176,12 +185,13 @@ __device__ __forceinline__ void record_timeout(FwdArgs const& a, volatile int* a
 // of its two Q tiles.  Causal: heads in groups of a.group; inside a group the
 // heaviest query blocks (the longest key ranges) come first, so taking items
 // in order approximates longest-processing-time-first while the K/V of the
-// heads in flight stay in L2.
+// heads in flight stay in L2.  (The host uses it too, to build the static
+// schedule.)
 struct FwdItem {
     int bh, q0[2], nkv[2], nmax;
 };
 
-__device__ __forceinline__ FwdItem fwd_item(const FwdArgs& a, int t) {
+__host__ __device__ __forceinline__ FwdItem fwd_item(const FwdArgs& a, int t) {
     FwdItem it;
     int qb;
     if (a.causal) {
@@ -198,28 +208,39 @@ __device__ __forceinline__ FwdItem fwd_item(const FwdArgs& a, int t) {
         if (it.q0[u] >= a.N) {
             it.nkv[u] = 0;  // tile beyond the sequence: inactive
         } else if (a.causal) {
-            it.nkv[u] = (min(it.q0[u] + kBM, a.N) - 1) / kBN + 1;
+            const int end = it.q0[u] + kBM < a.N ? it.q0[u] + kBM : a.N;
+            it.nkv[u] = (end - 1) / kBN + 1;
         } else {
             it.nkv[u] = n_kv_all;
         }
     }
-    it.nmax = max(it.nkv[0], it.nkv[1]);
+    it.nmax = it.nkv[0] > it.nkv[1] ? it.nkv[0] : it.nkv[1];
     return it;
 }
 
-// Next work item of this CTA: from the counter when the launch is persistent,
-// else the CTA's own block index once.
-__device__ __forceinline__ int fwd_fetch(const FwdArgs& a, int k, int n_items) {
-    const unsigned t = a.work ? atomicAdd(a.work, 1u)
-                              : (k == 0 ? blockIdx.x : static_cast<unsigned>(n_items));
-    return t < static_cast<unsigned>(n_items) ? static_cast<int>(t) : -1;
+// Next work item of this CTA: from the counter when there is one, else from
+// the static schedule in the launch parameters (Cap > 1), else round robin
+// (item k * grid + CTA; with one CTA per item that is the CTA's own item).
+template <int Cap>
+__device__ __forceinline__ int fwd_fetch(const FwdArgs& a, const FwdSched<Cap>& sc, int k,
+                                         int n_items) {
+    unsigned long long t;
+    if (a.work) {
+        t = atomicAdd(a.work, 1u);
+    } else if (Cap > 1) {
+        const int i = sc.start[blockIdx.x] + k;
+        t = i < sc.start[blockIdx.x + 1] ? sc.items[i] : static_cast<unsigned long long>(n_items);
+    } else {
+        t = static_cast<unsigned long long>(k) * gridDim.x + blockIdx.x;
+    }
+    return t < static_cast<unsigned long long>(n_items) ? static_cast<int>(t) : -1;
 }
 
-template <int HD>
+template <int HD, int Cap>
 __global__ void __launch_bounds__(kThreads, 1)
 fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
               const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
-              const FwdArgs args) {
+              const FwdArgs args, const __grid_constant__ FwdSched<Cap> sched) {
     using Cfg = FwdCfg<HD>;
     extern __shared__ uint8_t smem_raw[];
     FwdSmem<HD>& sm = *reinterpret_cast<FwdSmem<HD>*>(
@@ -281,7 +302,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                 if (k >= 2 && !(ok = mbar_wait(smem_u32(&sm.item_empty[slot]), ((k - 2) >> 1) & 1,
                                                kWaitTimeoutNs, abort)))
                     break;
-                const int item = fwd_fetch(args, k, n_items);
+                const int item = fwd_fetch(args, sched, k, n_items);
                 sm.item[slot] = item;
                 mbar_arrive(smem_u32(&sm.item_full[slot]));
                 if (item < 0) break;
@@ -738,23 +759,103 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
     }
 }
 
-template <int HD>
-cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                         const CUtensorMap& to, const FwdArgs& args, cudaStream_t stream) {
+// Static schedules of the forward without a work counter (FwdSched): a small
+// table for up to 512 items (1.5 KB of launch parameters), a large one for up
+// to 8192 (17 KB); beyond that, round robin.
+constexpr int kSchedSmall = 512;
+constexpr int kSchedLarge = 8192;
+
+// Greedy longest-first list scheduling of the items, in the counter's fetch
+// order, over `grid` CTAs: each item goes to the CTA whose modelled busy time
+// is least (lowest index on ties).  Item cost in half key steps (a key step:
+// one K/V tile against both Q tiles): FA_SCHED_STEP per step of the longer Q
+// tile plus FA_SCHED_FIXED for the Q loads and the O epilogue.
+#ifndef FA_SCHED_STEP
+#define FA_SCHED_STEP 2
+#endif
+#ifndef FA_SCHED_FIXED
+#define FA_SCHED_FIXED 2
+#endif
+template <int Cap>
+void build_schedule(const FwdArgs& a, int n_items, int grid, FwdSched<Cap>& sc) {
+    std::vector<std::vector<uint16_t>> lists(grid);
+    using Slot = std::pair<long long, int>;  // (busy time, CTA)
+    std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> free_at;
+    for (int c = 0; c < grid; ++c) free_at.push({0, c});
+    for (int t = 0; t < n_items; ++t) {
+        const FwdItem it = fwd_item(a, t);
+        const Slot s = free_at.top();
+        free_at.pop();
+        lists[s.second].push_back(static_cast<uint16_t>(t));
+        free_at.push({s.first + FA_SCHED_STEP * it.nmax + FA_SCHED_FIXED, s.second});
+    }
+    int pos = 0;
+    for (int c = 0; c < grid; ++c) {
+        sc.start[c] = static_cast<uint16_t>(pos);
+        for (uint16_t t : lists[c]) sc.items[pos++] = t;
+    }
+    for (int c = grid; c <= kFwdSchedMaxCtas; ++c) sc.start[c] = static_cast<uint16_t>(pos);
+}
+
+// Schedules already built, by the arguments that decide them (a launch with the
+// same sizes reuses its table).
+struct SchedKey {
+    int BH, N, n_qblk, group, group_last, causal, grid;
+    bool operator<(const SchedKey& o) const {
+        return std::tie(BH, N, n_qblk, group, group_last, causal, grid) <
+               std::tie(o.BH, o.N, o.n_qblk, o.group, o.group_last, o.causal, o.grid);
+    }
+};
+
+template <int Cap>
+const FwdSched<Cap>* cached_schedule(const FwdArgs& a, int n_items, int grid) {
+    static std::mutex mu;
+    static std::map<SchedKey, std::unique_ptr<FwdSched<Cap>>> cache;
+    const SchedKey key{a.BH, a.N, a.n_qblk, a.group, a.group_last, a.causal, grid};
+    std::lock_guard<std::mutex> lock(mu);
+    auto f = cache.find(key);
+    if (f != cache.end()) return f->second.get();
+    if (cache.size() >= 64) cache.clear();  // bounded; a cleared entry is rebuilt on demand
+    auto sc = std::make_unique<FwdSched<Cap>>();
+    build_schedule(a, n_items, grid, *sc);
+    return (cache[key] = std::move(sc)).get();
+}
+
+template <int HD, int Cap>
+cudaError_t launch_fwd_cap(unsigned grid, const CUtensorMap& tq, const CUtensorMap& tk,
+                           const CUtensorMap& tv, const CUtensorMap& to, const FwdArgs& args,
+                           const FwdSched<Cap>& sc, cudaStream_t stream) {
     const size_t smem = sizeof(FwdSmem<HD>) + 1024;
-    cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<HD>,
+    cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<HD, Cap>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    const long long items = static_cast<long long>(args.n_qblk) * args.BH;
-    unsigned grid = static_cast<unsigned>(items);
-    if (args.work) {
-        // persistent: one CTA per multiprocessor, work items handed out by a counter
-        if ((e = cudaMemsetAsync(args.work, 0, sizeof(unsigned), stream)) != cudaSuccess) return e;
-        grid = static_cast<unsigned>(items < args.sms ? items : args.sms);
-    }
-    fa_fwd_kernel<HD><<<grid, kThreads, smem, stream>>>(tq, tk, tv, to, args);
+    fa_fwd_kernel<HD, Cap><<<grid, kThreads, smem, stream>>>(tq, tk, tv, to, args, sc);
     return cudaGetLastError();
+}
+
+template <int HD>
+cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                         const CUtensorMap& to, const FwdArgs& args, cudaStream_t stream) {
+    const long long items = static_cast<long long>(args.n_qblk) * args.BH;
+    const int sms = args.sms < kFwdSchedMaxCtas ? args.sms : kFwdSchedMaxCtas;
+    // persistent either way: one CTA per multiprocessor (fewer for few items)
+    const unsigned grid = static_cast<unsigned>(items < sms ? items : sms);
+    static const FwdSched<1> none{};
+    if (args.work) {
+        // work items handed out by a counter in the caller's workspace
+        cudaError_t e = cudaMemsetAsync(args.work, 0, sizeof(unsigned), stream);
+        if (e != cudaSuccess) return e;
+        return launch_fwd_cap<HD, 1>(grid, tq, tk, tv, to, args, none, stream);
+    }
+    const int n = static_cast<int>(items);
+    if (items <= kSchedSmall)
+        return launch_fwd_cap<HD, kSchedSmall>(grid, tq, tk, tv, to, args,
+                                               *cached_schedule<kSchedSmall>(args, n, grid), stream);
+    if (items <= kSchedLarge)
+        return launch_fwd_cap<HD, kSchedLarge>(grid, tq, tk, tv, to, args,
+                                               *cached_schedule<kSchedLarge>(args, n, grid), stream);
+    return launch_fwd_cap<HD, 1>(grid, tq, tk, tv, to, args, none, stream);
 }
 
 }  // namespace

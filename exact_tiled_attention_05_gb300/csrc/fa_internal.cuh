@@ -46,8 +46,22 @@ struct FwdArgs {
     int causal;
     float scale_log2; // scale * log2(e)
     int* status;      // device status word
-    unsigned* work;   // work-item counter (zeroed before the launch), or null: one item per CTA
+    unsigned* work;   // work-item counter (zeroed before the launch), or null: a static
+                      // schedule (a table in the launch parameters, else round robin)
     int sms;          // multiprocessors of the device (grid of the persistent launch)
+};
+
+// Static schedule of the persistent forward when no work counter is given: CTA
+// c runs the items items[start[c]] .. items[start[c + 1] - 1] in that order.
+// It travels in the launch parameters, so concurrent launches share nothing.
+// The host fills it by greedy longest-first list scheduling over the item costs
+// in the counter's fetch order, i.e. what the counter does with modelled item
+// times.  Cap = 1 is the table-free launch (round robin: item k * grid + c).
+constexpr int kFwdSchedMaxCtas = 256;
+template <int Cap>
+struct FwdSched {
+    uint16_t start[kFwdSchedMaxCtas + 1];
+    uint16_t items[Cap];
 };
 
 // Causal work order of the persistent kernels: heads in groups of `group`
@@ -56,15 +70,15 @@ struct FwdArgs {
 // on.  The last group is larger so that its work, spread over all SMs, outlasts
 // its heaviest items, which then finish with the rest instead of after it.
 // Item t -> head bh and block rank (0 = heaviest).
-__device__ __forceinline__ void grouped_item(int t, int nblk, int BH, int group, int group_last,
-                                             int& bh, int& rank) {
+__host__ __device__ __forceinline__ void grouped_item(int t, int nblk, int BH, int group,
+                                                      int group_last, int& bh, int& rank) {
     const int n_reg = BH - group_last;  // heads in the regular groups
     const int t_reg = n_reg * nblk;
     int first, gc, r;
     if (t < t_reg) {
         const int grp = t / (group * nblk);
         first = grp * group;
-        gc = min(group, n_reg - first);
+        gc = group < n_reg - first ? group : n_reg - first;
         r = t - grp * group * nblk;
     } else {
         first = n_reg;

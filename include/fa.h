@@ -53,15 +53,18 @@ typedef enum {
  * softmax with a running max m and running sum l per row, unnormalised output
  * accumulator rescaled when the max moves, one normalisation O = acc / l at the
  * end, lse = m + ln l ("FlashAttention 1–4" §"FlashAttention (v1)" recurrence;
- * "07 GPU、资源估算与 FlashAttention" §7.8).  Each CTA computes one (head,
- * 256-row query block) work item; fa_fwd_ws below gives the same results
- * faster with a small workspace.  `stream` is a cudaStream_t. */
+ * "07 GPU、资源估算与 FlashAttention" §7.8).  Work items are (head, 256-row
+ * query block) pairs; one CTA per multiprocessor runs them back to back in a
+ * static schedule computed on the host (heaviest causal blocks first, greedy
+ * over the CTAs) and passed in the launch parameters, so the call needs no
+ * workspace and concurrent calls share nothing.  fa_fwd_ws below gives the
+ * same results with a work counter instead.  `stream` is a cudaStream_t. */
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
            int B, int H, int N, int d, float scale, int causal, void* stream);
 
 /* fa_fwd with a workspace holding a work counter: one CTA per multiprocessor
- * takes (head, 256-row query block) items until none are left, so the start-up
- * and epilogue of one item overlap the work of the next.  workspace:
+ * takes (head, 256-row query block) items from the counter until none are
+ * left (dynamic instead of fa_fwd's static schedule).  workspace:
  * caller-owned device memory of at least fa_fwd_workspace_size() bytes,
  * 256-byte aligned, contents on entry irrelevant; two calls that overlap on the
  * GPU must not share one.  NULL behaves as fa_fwd.  A workspace that is too

@@ -152,18 +152,30 @@ def test_many_heads_short_rows():
         check_lse(to_np(lse).reshape(l_ref.shape), l_ref, "many heads")
 
 
-@pytest.mark.parametrize("N,d,H", [(300, 128, 24), (1000, 64, 24), (4096, 128, 8)])
+@pytest.mark.parametrize("B,H,N,d", [
+    (2, 24, 300, 128), (2, 24, 1000, 64), (2, 8, 4096, 128),   # static table, up to 512 items
+    (2, 16, 8192, 128), (1, 32, 32768, 64),                    # static table, 1024 / 4096 items
+    (1, 9000, 128, 64),                                        # 9000 items: round robin
+])
 @pytest.mark.parametrize("causal", [False, True])
-def test_persistent_matches_one_item_per_cta(N, d, H, causal):
-    """With the work counter one CTA per SM runs many (head, query block) items
-    back to back; without it each CTA runs one.  Every item is computed by the
-    same code in the same order, so O and lse are bitwise equal."""
-    inp = wl.make_inputs(wl.WORKLOADS["single_head_256"], B=2, H=H, N=N, d=d, seed=N + d + causal)
+def test_static_schedule_matches_work_counter(B, H, N, d, causal):
+    """fa_fwd (no workspace) runs one CTA per SM over a static schedule (a
+    greedy longest-first table in the launch parameters, or round robin past
+    8192 items); fa_fwd_ws hands the items out from a counter.  Every item is
+    computed by the same code in the same order whichever CTA takes it, so O
+    and lse are bitwise equal: a missing or misrouted item would show."""
+    inp = wl.make_inputs(wl.WORKLOADS["single_head_256"], B=B, H=H, N=N, d=d, seed=N + d + causal)
     q, k, v = (inp[n].to(DEV) for n in ("q", "k", "v"))
     o1, l1 = fa.forward(q, k, v, causal=causal)
     o2, l2 = fa.forward(q, k, v, causal=causal, workspace=False)
     fa.sync_status()
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    if B * H > 1000:  # the round-robin case: a few heads against the oracle too
+        heads = [0, 4499, B * H - 1]
+        o_ref, l_ref = oracle.fwd(bits(inp["q"]), bits(inp["k"]), bits(inp["v"]), 1 / math.sqrt(d),
+                                  causal, heads=heads)
+        check_o_beyond_rounding(to_np(o2).reshape(B * H, N, d)[heads], o_ref, "round robin")
+        check_lse(to_np(l2).reshape(B * H, N)[heads], l_ref, "round robin")
 
 
 def test_persistent_calls_on_two_streams():

@@ -279,17 +279,21 @@ def attention_on_codes_rows(quant, scale: float, causal: bool, rows, tile: int =
 
 
 def ideal_fp8_error(o_exact: np.ndarray, quant, scale: float, causal: bool, tile: int = 128,
-                    rows=None):
+                    rows=None, lse_exact=None):
     """The method's own FP8 error: exact attention on the exactly rounded codes
     (``attention_on_codes``) against exact attention on the original inputs
     (o_exact, [BH, N, d], or [BH, R, d] for the query rows ``rows``).
-    Returns (rmse, max |err|)."""
+    Returns (rmse, max |err|), and max |lse error| third when lse_exact
+    (the exact attention's lse, [BH, N] or [BH, R]) is given."""
     if rows is None:
-        o_codes, _ = attention_on_codes(quant, scale, causal, tile)
+        o_codes, lse_codes = attention_on_codes(quant, scale, causal, tile)
     else:
-        o_codes, _ = attention_on_codes_rows(quant, scale, causal, rows, tile)
+        o_codes, lse_codes = attention_on_codes_rows(quant, scale, causal, rows, tile)
     err = np.abs(o_codes - o_exact)
-    return float(np.sqrt((err ** 2).mean())), float(err.max())
+    out = (float(np.sqrt((err ** 2).mean())), float(err.max()))
+    if lse_exact is not None:
+        out += (float(np.abs(lse_codes - lse_exact).max()),)
+    return out
 
 
 def fp8_budget(o_exact: np.ndarray, ideal):
@@ -304,6 +308,14 @@ def fp8_budget(o_exact: np.ndarray, ideal):
     a = np.maximum(np.abs(o_exact), np.finfo(np.float32).tiny)
     half = np.ldexp(1.0, (np.floor(np.log2(a)) - 8).astype(np.int64))
     return 2.0 * ideal[0] + float(np.sqrt((half ** 2).mean())), 2.0 * ideal[1] + half
+
+
+def fp8_lse_budget(ideal_lse_max: float) -> float:
+    """The FP8 forward's lse budget against exact attention on the original
+    inputs: its probabilities are not rounded for the row sums, so only the
+    quantized scores move lse; 2 x the method's own largest lse error plus
+    the 1e-3 of the bf16 path's lse gate."""
+    return 2.0 * ideal_lse_max + 1e-3
 
 
 # E4M3 rounding of a probability y = P * c: |e4m3(y) - y| <= max(2^-4 y, 2^-10)
@@ -368,16 +380,14 @@ def p_rounding_bound(quant, scale: float, causal: bool, tile: int = 128, rows=No
     return bound, o_ref, lse
 
 
-def band_slack(quant, scale: float, causal: bool, tile: int = 128, rows=None):
-    """Diagnostic companion of ``p_rounding_bound``: where an element's band
-    straddles a rounding boundary, an implementation may hold the neighbouring
-    code, one E4M3 step (times the tile scale, widened by the scale tolerance)
-    away from the exact code.  Per query row i this moves each score by at most
-    ds_ij = scale (sum_c U_q[i,c] |k_jc| + |q_ic| U_k[j,c]) (U: those steps,
-    0 elsewhere; |q|, |k| widened by U), so the weights change by at most a
-    factor exp(+-2 max_j ds_ij), and O moves by at most
-    (exp(2 max_j ds_ij) - 1) max_j |v_j - O_i| + sum_j P_ij U_v[j] / (1 - ...).
-    Returns [BH, R, d] (all rows when rows is None)."""
+def band_score_slack(quant, scale: float, causal: bool, tile: int = 128, rows=None):
+    """Per query row, the largest change of any visible score s_ij that the band
+    cases' neighbouring codes can cause, max_j ds_ij (see ``band_slack``); an
+    lse moves by no more than that.  Returns [BH, R]."""
+    return _band_terms(quant, scale, causal, tile, rows)[0]
+
+
+def _band_terms(quant, scale, causal, tile, rows):
     qd, kd, vd = dequantized_qkv(quant, tile)
     BH, N, d = qd.shape
 
@@ -392,6 +402,7 @@ def band_slack(quant, scale: float, causal: bool, tile: int = 128, rows=None):
     if rows is None:
         rows = np.tile(np.arange(N), (BH, 1))
     rows = np.asarray(rows, np.int64)
+    dmax_all = np.empty((BH, rows.shape[1]))
     out = np.empty((BH, rows.shape[1], d))
     for b in range(BH):
         qa = np.abs(qd[b][rows[b]]) + uq[b][rows[b]]
@@ -409,5 +420,19 @@ def band_slack(quant, scale: float, causal: bool, tile: int = 128, rows=None):
         growth = np.exp(2 * dmax) - 1.0
         spread = np.stack([np.where(vis[i][:, None], np.abs(vd[b] - o[i][None, :]), 0.0).max(axis=0)
                            for i in range(len(rows[b]))])       # [R, d]
+        dmax_all[b] = dmax
         out[b] = growth[:, None] * spread + (p @ uv[b]) * (1.0 + growth[:, None])
-    return out
+    return dmax_all, out
+
+
+def band_slack(quant, scale: float, causal: bool, tile: int = 128, rows=None):
+    """Diagnostic companion of ``p_rounding_bound``: where an element's band
+    straddles a rounding boundary, an implementation may hold the neighbouring
+    code, one E4M3 step (times the tile scale, widened by the scale tolerance)
+    away from the exact code.  Per query row i this moves each score by at most
+    ds_ij = scale (sum_c U_q[i,c] |k_jc| + |q_ic| U_k[j,c]) (U: those steps,
+    0 elsewhere; |q|, |k| widened by U), so the weights change by at most a
+    factor exp(+-2 max_j ds_ij), and O moves by at most
+    (exp(2 max_j ds_ij) - 1) max_j |v_j - O_i| + exp(2 max_j ds_ij) sum_j P_ij U_v[j].
+    Returns [BH, R, d] (all rows when rows is None)."""
+    return _band_terms(quant, scale, causal, tile, rows)[1]

@@ -78,16 +78,19 @@ def check_scales(got, ref, name):
 
 
 def exact_attention(inp, causal, rows=None):
-    """Exact attention (fp64 oracle) on the original bf16 inputs."""
+    """Exact attention (fp64 oracle) on the original bf16 inputs: (o, lse)."""
     q, k, v = bits(inp["q"]), bits(inp["k"]), bits(inp["v"])
     if rows is None:
-        return oracle.fwd(q, k, v, 1.0 / math.sqrt(D), causal)[0]
-    return oracle.fwd_rows(q, k, v, 1.0 / math.sqrt(D), causal, rows)[0]
+        return oracle.fwd(q, k, v, 1.0 / math.sqrt(D), causal)
+    return oracle.fwd_rows(q, k, v, 1.0 / math.sqrt(D), causal, rows)
 
 
-def check_budget(o, o_exact, quant, causal, what, rows=None):
-    """The FP8 O gate against exact attention on the original inputs."""
-    ideal = ofp8.ideal_fp8_error(o_exact, quant, 1.0 / math.sqrt(D), causal, rows=rows)
+def check_budget(o, lse, exact, quant, causal, what, rows=None):
+    """The FP8 gates against exact attention on the original inputs: O within
+    its RMSE and element-wise budgets, lse within its budget."""
+    o_exact, lse_exact = exact
+    ideal = ofp8.ideal_fp8_error(o_exact, quant, 1.0 / math.sqrt(D), causal, rows=rows,
+                                 lse_exact=lse_exact)
     rmse_b, max_b = ofp8.fp8_budget(o_exact, ideal)
     err = np.abs(o - o_exact)
     rmse = float(np.sqrt((err ** 2).mean()))
@@ -96,13 +99,18 @@ def check_budget(o, o_exact, quant, causal, what, rows=None):
     worst = (err - max_b).max()
     assert worst <= 0, (f"{what}: max err {err.max():.3e} over its budget by {worst:.3e} "
                         f"(ideal max {ideal[1]:.3e})")
+    if lse is not None:
+        lerr = np.abs(lse - lse_exact).max()
+        assert lerr <= ofp8.fp8_lse_budget(ideal[2]), (
+            f"{what}: lse max err {lerr:.3e} over its budget (ideal {ideal[2]:.3e})")
     return rmse, ideal
 
 
-def check_diagnostic(o, quant, causal, what, rows=None):
+def check_diagnostic(o, lse, quant, causal, what, rows=None):
     """O within the P-rounding bound (plus band slack, bf16 rounding and fp32
-    score arithmetic) of exact attention on the oracle's codes; the typical
-    error well inside it."""
+    score arithmetic) of exact attention on the oracle's codes, the typical
+    error well inside it; lse within 1e-3 plus the band cases' largest score
+    change of the same attention's lse."""
     scale = 1.0 / math.sqrt(D)
     bound, o_ref, lse_ref = ofp8.p_rounding_bound(quant, scale, causal, rows=rows)
     slack = (ofp8.band_slack(quant, scale, causal, rows=rows) + bf16_half_ulp(o_ref)
@@ -112,7 +120,12 @@ def check_diagnostic(o, quant, causal, what, rows=None):
     assert excess.max() <= 0, (
         f"{what}: max err {err.max():.3e} exceeds the P-rounding bound by {excess.max():.3e}")
     assert err.mean() <= 0.5 * bound.mean() + 1e-6
-    return lse_ref
+    if lse is not None:
+        lerr = np.abs(lse - lse_ref)
+        ds = ofp8.band_score_slack(quant, scale, causal, rows=rows)
+        assert np.isfinite(lse).all(), f"{what}: non-finite lse"
+        assert (lerr - ds).max() <= 1e-3, (
+            f"{what}: lse max err {lerr.max():.3e}, beyond the band slack by {(lerr - ds).max():.3e}")
 
 
 QUANT_CASES = [
@@ -197,9 +210,8 @@ def test_fp8_forward_parity(B, H, N, causal, rotate, per_tensor):
     inp, words, o, lse = fp8_case(B, H, N, causal, rotate, per_tensor, seed=N)
     quant = oracle_quant(inp, words, rotate, per_tensor)
     what = f"fp8 B={B} H={H} N={N} causal={causal} rotate={rotate} per_tensor={per_tensor}"
-    rmse, ideal = check_budget(o, exact_attention(inp, causal), quant, causal, what)
-    lse_ref = check_diagnostic(o, quant, causal, what)
-    check_lse(lse, lse_ref, what)
+    rmse, ideal = check_budget(o, lse, exact_attention(inp, causal), quant, causal, what)
+    check_diagnostic(o, lse, quant, causal, what)
     print(f"\n{what}: RMSE vs exact attention {rmse:.3e} (method's own {ideal[0]:.3e})")
 
 
@@ -224,10 +236,9 @@ def test_fp8_full_size_sampled_rows():
     lse = to_np(lse).reshape(w.BH, w.N)
     got = np.stack([o[b][rows[b]] for b in range(w.BH)])
     got_l = np.stack([lse[b][rows[b]] for b in range(w.BH)])
-    rmse, ideal = check_budget(got, exact_attention(inp, True, rows), quant, True,
+    rmse, ideal = check_budget(got, got_l, exact_attention(inp, True, rows), quant, True,
                                "fp8 full size", rows=rows)
-    lse_ref = check_diagnostic(got, quant, True, "fp8 full size", rows=rows)
-    check_lse(got_l, lse_ref, "fp8 full size lse")
+    check_diagnostic(got, got_l, quant, True, "fp8 full size", rows=rows)
     print(f"\nfp8 full size: {n_band} band codes; RMSE vs exact attention {rmse:.3e} "
           f"(method's own {ideal[0]:.3e})")
 
@@ -278,7 +289,8 @@ def rmse_modes(kind, B=1, H=4, N=2048, causal=True, seed=21):
     budget (twice the error of exact attention on its exactly rounded codes)."""
     inp = wl.outlier_inputs(B, H, N, D, seed=seed, kind=kind)
     q, k, v = (inp[n].to(DEV) for n in ("q", "k", "v"))
-    o_ref = exact_attention(inp, causal)
+    exact = exact_attention(inp, causal)
+    o_ref = exact[0]
     words = wl.sign_bits(seed + 1)
     out, ideal = {}, {}
     for name, rot, pt in (("tile+rotate", True, False), ("tile", False, False),
@@ -286,7 +298,7 @@ def rmse_modes(kind, B=1, H=4, N=2048, causal=True, seed=21):
         o = to_np(fa.forward_fp8(q, k, v, signs=words, causal=causal, rotate=rot,
                                  per_tensor=pt)[0]).reshape(o_ref.shape)
         quant = oracle_quant(inp, words, rot, pt)
-        out[name], ideal[name] = check_budget(o, o_ref, quant, causal, f"'{kind}' {name}")
+        out[name], ideal[name] = check_budget(o, None, exact, quant, causal, f"'{kind}' {name}")
     o16 = fa.forward(q, k, v, causal=causal)[0]
     out["bf16"] = float(np.sqrt(((to_np(o16).reshape(o_ref.shape) - o_ref) ** 2).mean()))
     fa.sync_status()
@@ -325,7 +337,6 @@ def test_fp8_largest_head_count():
     base = torch.arange(B * H, device=DEV) % nb
     assert torch.equal(o, o[:nb][base]) and torch.equal(lse, lse[:nb][base])
     quant = oracle_quant(inp, words, True, False)
-    got = to_np(o[:nb])
-    check_budget(got, exact_attention(inp, True), quant, True, "fp8, 65535 heads")
-    lse_ref = check_diagnostic(got, quant, True, "fp8, 65535 heads")
-    check_lse(to_np(lse[:nb]), lse_ref, "fp8 lse, 65535 heads")
+    got, got_l = to_np(o[:nb]), to_np(lse[:nb])
+    check_budget(got, got_l, exact_attention(inp, True), quant, True, "fp8, 65535 heads")
+    check_diagnostic(got, got_l, quant, True, "fp8, 65535 heads")

@@ -474,11 +474,15 @@ def test_band_slack_covers_neighbour_codes():
         n_flip += int(amb.sum())
         flipped[n] = dict(ref, codes=np.where(amb, fp8.e4m3_encode(other), ref["codes"]).astype(np.uint8))
     assert n_flip > 0
-    o0, _ = fp8.attention_on_codes(quant, 0.09, True)
-    o1, _ = fp8.attention_on_codes(flipped, 0.09, True)
+    o0, l0 = fp8.attention_on_codes(quant, 0.09, True)
+    o1, l1 = fp8.attention_on_codes(flipped, 0.09, True)
     slack = fp8.band_slack(quant, 0.09, True)
     assert np.all(np.abs(o1 - o0) <= slack * (1 + 1e-9) + 1e-15)
     assert (np.abs(o1 - o0)).max() > 0
+    # and lse moves by no more than the largest score change of its row
+    ds = fp8.band_score_slack(quant, 0.09, True)
+    assert np.all(np.abs(l1 - l0) <= ds * (1 + 1e-9) + 1e-15)
+    assert (np.abs(l1 - l0)).max() > 0
 
 
 def test_budget_of_exact_codes_is_met_by_exact_codes():

@@ -16,6 +16,13 @@ using namespace ptx;
 // ---------------------------------------------------------------------------
 template <int HD>
 __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const BwdArgs a) {
+    // Within fa_bwd the dK/dV and dQ kernels that follow skip the memsets of
+    // their work counters: this kernel zeroes them (the stream runs the two
+    // kernels after it).
+    if (a.zero_counters && blockIdx.x == 0 && threadIdx.x == 0) {
+        a.work[kWorkDkdv] = 0u;
+        a.work[kWorkDq] = 0u;
+    }
     constexpr int kTPR = HD / 8;       // threads per row, one 16-byte vector (8 bf16) each
     constexpr int kRPW = 32 / kTPR;    // rows per warp pass
     constexpr int kUnroll = 4;         // passes whose loads are in flight together
@@ -128,7 +135,9 @@ struct alignas(1024) BwdSmem {
     uint64_t q_full[BwdCfg<HD>::kQSlots];    // Q tile and its lse * log2(e) landed
     uint64_t q_empty[BwdCfg<HD>::kQSlots];   // after dK(i); an item's last slot after its dK store
     uint64_t do_full[BwdCfg<HD>::kDoSlots];  // dO tile and its D landed
-    uint64_t do_empty[BwdCfg<HD>::kDoSlots]; // after dV(i); an item's last slot after its dV store
+    uint64_t do_empty[BwdCfg<HD>::kDoSlots]; // dO tile and its D free: after dV(i) (an item's last
+                                             // slot: after its dV store) and after every compute
+                                             // thread has read D in its dS phase
     uint64_t p_ready[2];  // P^T for each thread's queries 0-31, then 32-63
     uint64_t s_full, dp_full, ds_ready, dkdv_done, drain;
     uint64_t out_staged;  // every compute thread has staged its dV / dK row (per item)
@@ -203,7 +212,7 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         }
         for (int s = 0; s < Cfg::kDoSlots; ++s) {
             mbar_init(smem_u32(&sm.do_full[s]), 1);
-            mbar_init(smem_u32(&sm.do_empty[s]), 1);
+            mbar_init(smem_u32(&sm.do_empty[s]), 1 + kBCompute);
         }
         mbar_init(smem_u32(&sm.s_full), 1);
         mbar_init(smem_u32(&sm.dp_full), 1);
@@ -558,6 +567,10 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                     }
                 }
             }
+            // D of this slot has been read: with the dV MMA's commit (or the dV
+            // store, for an item's last tile) this frees the slot for the next dO
+            // tile and its D.
+            mbar_arrive(smem_u32(&sm.do_empty[ds]));
             // dS^T over the first 32 of the 64 dP^T columns this thread read
             tmem_st32(lane_addr + Cfg::kDP + wg * 64, pk);
             tmem_wait_st();
@@ -623,12 +636,13 @@ cudaError_t launch_bwd_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, cons
                               const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
                               const BwdArgs& a, cudaStream_t stream) {
     const size_t smem = sizeof(BwdSmem<HD>);
-    cudaError_t e = cudaFuncSetAttribute(fa_bwd_dkdv_kernel<HD>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    cudaError_t e = smem_limit_once<fa_bwd_dkdv_kernel<HD>>(static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     // persistent: one CTA per multiprocessor, work items handed out by a counter
-    if ((e = cudaMemsetAsync(a.work + kWorkDkdv, 0, sizeof(unsigned), stream)) != cudaSuccess) return e;
+    // (zeroed here, or by the prep kernel just before inside fa_bwd)
+    if (!a.counters_zeroed &&
+        (e = cudaMemsetAsync(a.work + kWorkDkdv, 0, sizeof(unsigned), stream)) != cudaSuccess)
+        return e;
     const long long items = static_cast<long long>(a.n_kblk) * a.BH;
     const unsigned grid = static_cast<unsigned>(items < a.sms ? items : a.sms);
     fa_bwd_dkdv_kernel<HD><<<grid, kBThreads, smem, stream>>>(tq, tk, tv, tdo, tdk, tdv, a);

@@ -315,3 +315,29 @@ def test_long_sequence_non_causal_key_rows():
     check_grad(take(dq, qrows), g[0], "dq sampled rows N=2^15")
     check_grad(take(dk, krows), g[1], "dk sampled key rows N=2^15")
     check_grad(take(dv, krows), g[2], "dv sampled key rows N=2^15")
+
+
+def test_backward_bitwise_repeatable_back_to_back():
+    """16 forward + backward passes of the fwd+bwd workload enqueued back to back
+    on one stream (fresh output buffers each, no host synchronisation between
+    them): every pass's dQ, dK and dV equal the first pass's bit for bit.  The
+    dK/dV kernel's dO ring slots also hold each tile's D, which its compute
+    threads read in the dS phase; a slot may be refilled only after both the dV
+    product and those reads (releasing it after dV alone let dK pick up the
+    next tile's D, now and then, with back-to-back launches)."""
+    w = wl.WORKLOADS["fwdbwd_4k_d128"]
+    inp = wl.make_inputs(w)
+    q, k, v, do = (inp[n].to(DEV) for n in ("q", "k", "v", "do"))
+    ws = fa.alloc_workspace(w.B, w.H, w.N, w.d, DEV)
+    outs = []
+    for _ in range(16):
+        o, lse = fa.forward(q, k, v, causal=True)
+        dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+        fa.backward(q, k, v, o, lse, do, causal=True, dq=dq, dk=dk, dv=dv, workspace=ws)
+        outs.append((dq, dk, dv))
+    fa.sync_status()
+    for n, (dq, dk, dv) in enumerate(outs[1:], 1):
+        for got, ref, name in ((dq, outs[0][0], "dq"), (dk, outs[0][1], "dk"), (dv, outs[0][2], "dv")):
+            if not torch.equal(got, ref):
+                heads = torch.nonzero((got != ref).reshape(w.BH, -1).any(dim=1)).flatten().tolist()
+                raise AssertionError(f"pass {n}: {name} differs from the first pass in heads {heads[:10]}")

@@ -278,24 +278,29 @@ def run_gpu(args, world, rank, local):
         if rc != 0:
             raise RuntimeError(f"{what}: {fa.status_string(rc)}")
 
-    def step(ev=None):
-        if ev:
-            ev[0].record(stream)
+    def step():
+        # one step through the public calls: the forward, then the backward
+        # (fa_bwd runs prep, dK/dV and dQ)
         check(fa.fa_fwd_ws(P(q), P(k), P(v), P(o), P(lse), B, H, N, d, scale, 1, P(fws), fws.numel(),
                            h), "fa_fwd_ws")
-        if ev:
-            ev[1].record(stream)
+        check(fa.fa_bwd(P(q), P(k), P(v), P(o), P(lse), P(do), P(dq), P(dk), P(dv), B, H, N, d, scale,
+                        1, P(ws), ws.numel(), h), "fa_bwd")
+
+    def step_staged(ev):
+        # the same step with the backward's three stages called one by one and
+        # CUDA events between the four kernels
+        ev[0].record(stream)
+        check(fa.fa_fwd_ws(P(q), P(k), P(v), P(o), P(lse), B, H, N, d, scale, 1, P(fws), fws.numel(),
+                           h), "fa_fwd_ws")
+        ev[1].record(stream)
         check(fa.fa_bwd_prep(P(o), P(do), P(lse), B, H, N, d, P(ws), ws.numel(), h), "fa_bwd_prep")
-        if ev:
-            ev[2].record(stream)
+        ev[2].record(stream)
         check(fa.fa_bwd_main(P(q), P(k), P(v), P(lse), P(do), P(dk), P(dv), B, H, N, d, scale, 1,
                              P(ws), ws.numel(), h), "fa_bwd_main")
-        if ev:
-            ev[3].record(stream)
+        ev[3].record(stream)
         check(fa.fa_bwd_dq(P(q), P(k), P(v), P(lse), P(do), P(dq), B, H, N, d, scale, 1, P(ws),
                            ws.numel(), h), "fa_bwd_dq")
-        if ev:
-            ev[4].record(stream)
+        ev[4].record(stream)
 
     for _ in range(args.warmup):
         step()
@@ -303,7 +308,6 @@ def run_gpu(args, world, rank, local):
     check(fa.fa_sync_status(h), "warm-up")
 
     # ---------------- timed region: K steps on resident inputs ----------------
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     clocks = ClockSampler(local)
     clocks.start()
     barrier(world)
@@ -312,7 +316,7 @@ def run_gpu(args, world, rank, local):
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
     for i in range(args.steps):
-        step(evs[i])
+        step()
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
@@ -320,7 +324,18 @@ def run_gpu(args, world, rank, local):
     check(fa.fa_sync_status(h), "timed region")
     elapsed_ms = t_start.elapsed_time(t_end)
     elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
-    per = {name: sum(e[a].elapsed_time(e[b]) for e in evs) / args.steps
+
+    # ---------------- per-kernel times: the staged step, events between kernels ----------------
+    # (each interval includes its kernel's launch gap and, for the stages called
+    # on their own, the memset of their work counter)
+    n_staged = max(3, min(args.steps, 200))
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n_staged)]
+    torch.cuda.synchronize(dev)
+    for i in range(n_staged):
+        step_staged(evs[i])
+    torch.cuda.synchronize(dev)
+    check(fa.fa_sync_status(h), "staged steps")
+    per = {name: sum(e[a].elapsed_time(e[b]) for e in evs) / n_staged
            for name, a, b in (("fwd", 0, 1), ("bwd_prep", 1, 2), ("bwd_dkdv", 2, 3),
                               ("bwd_dq", 3, 4))}
     f_fwd = fwd_flops(w)
@@ -505,7 +520,8 @@ def run_gpu(args, world, rank, local):
         "pct_of_bf16_peak": 100.0 * value / world / peak_burst,
         "peak_bf16_tflops": peak_burst, "peak_source": peak_src,
         "step": step_line, "sustained": sustained,
-        "kernel_ms": per, "kernels": kernels, "roofline": roofline, "e2e": e2e,
+        "kernel_ms": per, "kernel_ms_steps": n_staged, "kernels": kernels, "roofline": roofline,
+        "e2e": e2e,
         "gpu_launches": 4 * args.steps,
         "clocks": clk, "forward_gate": fwd_gate, "forward_gate_long": fwd_long,
         "forward_d64": fwd_d64, "forward_single_head": fwd_single, "fp8_forward": fp8,

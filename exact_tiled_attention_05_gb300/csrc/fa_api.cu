@@ -277,6 +277,60 @@ int bwd_maps(BwdArgs& a, CUtensorMap* maps, const void* q, const void* k, const 
     return kOk;
 }
 
+// The three backward stages.  Inside fa_bwd (fused = true) prep zeroes the
+// dK/dV and dQ work counters and those two kernels skip their memsets; called
+// on their own, each stage zeroes its own counter.
+int bwd_prep_impl(const void* o, const void* dout, const float* lse, int B, int H, int N, int d,
+                  void* workspace, size_t workspace_bytes, void* stream, bool fused) {
+    if (!o || !dout || !lse) return kErrInvalidArg;
+    BwdArgs a{};
+    int rc = bwd_common(a, B, H, N, d, 1.f, 0, workspace, workspace_bytes);
+    if (rc) return rc;
+    if (!aligned16(o) || !aligned16(dout) || (reinterpret_cast<uintptr_t>(lse) & 3u))
+        return kErrMisaligned;
+    a.o = o;
+    a.dout = dout;
+    a.lse = lse;
+    a.zero_counters = fused ? 1 : 0;
+    return map_cuda(launch_bwd_prep(d, a, static_cast<cudaStream_t>(stream)));
+}
+
+int bwd_main_impl(const void* q, const void* k, const void* v, const float* lse, const void* dout,
+                  void* dk, void* dv, int B, int H, int N, int d, float scale, int causal,
+                  void* workspace, size_t workspace_bytes, void* stream, bool fused) {
+    if (!q || !k || !v || !lse || !dout || !dk || !dv) return kErrInvalidArg;
+    BwdArgs a{};
+    CUtensorMap m[4];
+    int rc = bwd_maps(a, m, q, k, v, lse, dout, B, H, N, d, scale, causal, workspace,
+                      workspace_bytes);
+    if (rc) return rc;
+    if (!aligned16(dk) || !aligned16(dv)) return kErrMisaligned;
+    a.dk = dk;
+    a.dv = dv;
+    a.counters_zeroed = fused ? 1 : 0;
+    CUtensorMap tdk, tdv;
+    if ((rc = make_map(&tdk, dk, B * H, N, d)) || (rc = make_map(&tdv, dv, B * H, N, d))) return rc;
+    return map_cuda(
+        launch_bwd_dkdv(d, m[0], m[1], m[2], m[3], tdk, tdv, a, static_cast<cudaStream_t>(stream)));
+}
+
+int bwd_dq_impl(const void* q, const void* k, const void* v, const float* lse, const void* dout,
+                void* dq, int B, int H, int N, int d, float scale, int causal, void* workspace,
+                size_t workspace_bytes, void* stream, bool fused) {
+    if (!q || !k || !v || !lse || !dout || !dq) return kErrInvalidArg;
+    BwdArgs a{};
+    CUtensorMap m[4];
+    int rc = bwd_maps(a, m, q, k, v, lse, dout, B, H, N, d, scale, causal, workspace,
+                      workspace_bytes);
+    if (rc) return rc;
+    if (!aligned16(dq)) return kErrMisaligned;
+    a.dq = dq;
+    a.counters_zeroed = fused ? 1 : 0;
+    CUtensorMap tdq;
+    if ((rc = make_map(&tdq, dq, B * H, N, d))) return rc;
+    return map_cuda(launch_bwd_dq(d, m[0], m[1], m[2], m[3], tdq, a, static_cast<cudaStream_t>(stream)));
+}
+
 }  // namespace
 }  // namespace fa
 
@@ -351,50 +405,21 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
 
 int fa_bwd_prep(const void* o, const void* dout, const float* lse, int B, int H, int N, int d,
                 void* workspace, size_t workspace_bytes, void* stream) {
-    if (!o || !dout || !lse) return FA_ERR_INVALID_ARG;
-    BwdArgs a{};
-    int rc = bwd_common(a, B, H, N, d, 1.f, 0, workspace, workspace_bytes);
-    if (rc) return rc;
-    if (!aligned16(o) || !aligned16(dout) || (reinterpret_cast<uintptr_t>(lse) & 3u))
-        return FA_ERR_MISALIGNED;
-    a.o = o;
-    a.dout = dout;
-    a.lse = lse;
-    return map_cuda(launch_bwd_prep(d, a, static_cast<cudaStream_t>(stream)));
+    return bwd_prep_impl(o, dout, lse, B, H, N, d, workspace, workspace_bytes, stream, false);
 }
 
 int fa_bwd_main(const void* q, const void* k, const void* v, const float* lse, const void* dout,
                 void* dk, void* dv, int B, int H, int N, int d, float scale, int causal,
                 void* workspace, size_t workspace_bytes, void* stream) {
-    if (!q || !k || !v || !lse || !dout || !dk || !dv) return FA_ERR_INVALID_ARG;
-    BwdArgs a{};
-    CUtensorMap m[4];
-    int rc = bwd_maps(a, m, q, k, v, lse, dout, B, H, N, d, scale, causal, workspace,
-                      workspace_bytes);
-    if (rc) return rc;
-    if (!aligned16(dk) || !aligned16(dv)) return FA_ERR_MISALIGNED;
-    a.dk = dk;
-    a.dv = dv;
-    CUtensorMap tdk, tdv;
-    if ((rc = make_map(&tdk, dk, B * H, N, d)) || (rc = make_map(&tdv, dv, B * H, N, d))) return rc;
-    return map_cuda(
-        launch_bwd_dkdv(d, m[0], m[1], m[2], m[3], tdk, tdv, a, static_cast<cudaStream_t>(stream)));
+    return bwd_main_impl(q, k, v, lse, dout, dk, dv, B, H, N, d, scale, causal, workspace,
+                         workspace_bytes, stream, false);
 }
 
 int fa_bwd_dq(const void* q, const void* k, const void* v, const float* lse, const void* dout,
               void* dq, int B, int H, int N, int d, float scale, int causal, void* workspace,
               size_t workspace_bytes, void* stream) {
-    if (!q || !k || !v || !lse || !dout || !dq) return FA_ERR_INVALID_ARG;
-    BwdArgs a{};
-    CUtensorMap m[4];
-    int rc = bwd_maps(a, m, q, k, v, lse, dout, B, H, N, d, scale, causal, workspace,
-                      workspace_bytes);
-    if (rc) return rc;
-    if (!aligned16(dq)) return FA_ERR_MISALIGNED;
-    a.dq = dq;
-    CUtensorMap tdq;
-    if ((rc = make_map(&tdq, dq, B * H, N, d))) return rc;
-    return map_cuda(launch_bwd_dq(d, m[0], m[1], m[2], m[3], tdq, a, static_cast<cudaStream_t>(stream)));
+    return bwd_dq_impl(q, k, v, lse, dout, dq, B, H, N, d, scale, causal, workspace,
+                       workspace_bytes, stream, false);
 }
 
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
@@ -403,12 +428,14 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
     if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
     int rc = check_shape(B, H, N, d, scale, causal);
     if (rc) return rc;
-    if ((rc = fa_bwd_prep(o, dout, lse, B, H, N, d, workspace, workspace_bytes, stream))) return rc;
-    if ((rc = fa_bwd_main(q, k, v, lse, dout, dk, dv, B, H, N, d, scale, causal, workspace,
-                          workspace_bytes, stream)))
+    // prep zeroes the two work counters, so the kernels after it need no memsets
+    if ((rc = bwd_prep_impl(o, dout, lse, B, H, N, d, workspace, workspace_bytes, stream, true)))
         return rc;
-    return fa_bwd_dq(q, k, v, lse, dout, dq, B, H, N, d, scale, causal, workspace, workspace_bytes,
-                     stream);
+    if ((rc = bwd_main_impl(q, k, v, lse, dout, dk, dv, B, H, N, d, scale, causal, workspace,
+                            workspace_bytes, stream, true)))
+        return rc;
+    return bwd_dq_impl(q, k, v, lse, dout, dq, B, H, N, d, scale, causal, workspace, workspace_bytes,
+                       stream, true);
 }
 
 size_t fa_fp8_workspace_size(int B, int H, int N, int d) {

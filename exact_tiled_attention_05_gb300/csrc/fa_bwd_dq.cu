@@ -498,12 +498,13 @@ cudaError_t launch_bwd_dq_t(const CUtensorMap& tq, const CUtensorMap& tk, const 
                             const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a,
                             cudaStream_t stream) {
     const size_t smem = sizeof(DqSmem<HD>);
-    cudaError_t e = cudaFuncSetAttribute(fa_bwd_dq_kernel<HD>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    cudaError_t e = smem_limit_once<fa_bwd_dq_kernel<HD>>(static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     // persistent: one CTA per multiprocessor, work items handed out by a counter
-    if ((e = cudaMemsetAsync(a.work + kWorkDq, 0, sizeof(unsigned), stream)) != cudaSuccess) return e;
+    // (zeroed here, or by the prep kernel inside fa_bwd)
+    if (!a.counters_zeroed &&
+        (e = cudaMemsetAsync(a.work + kWorkDq, 0, sizeof(unsigned), stream)) != cudaSuccess)
+        return e;
     const long long items = static_cast<long long>(a.n_kblk) * a.BH;
     const unsigned grid = static_cast<unsigned>(items < a.sms ? items : a.sms);
     fa_bwd_dq_kernel<HD><<<grid, kQThreads, smem, stream>>>(tq, tk, tv, tdo, tdq, a);

@@ -792,8 +792,7 @@ fa_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
 
 cudaError_t launch_fp8_quant(const Fp8Args& a, cudaStream_t stream) {
     const size_t smem_v = 128 * 130 * sizeof(uint16_t);
-    cudaError_t e = cudaFuncSetAttribute(fa_fp8_quant_v_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem_v));
+    cudaError_t e = smem_limit_once<fa_fp8_quant_v_kernel<1>>(static_cast<int>(smem_v));
     if (e != cudaSuccess) return e;
     const dim3 grid_qk(static_cast<unsigned>(a.n_tiles), static_cast<unsigned>(a.BH), 2);
     const dim3 grid_v(static_cast<unsigned>(a.n_tiles), static_cast<unsigned>(a.BH), 1);
@@ -813,8 +812,7 @@ cudaError_t launch_fp8_quant(const Fp8Args& a, cudaStream_t stream) {
 cudaError_t launch_fwd_fp8(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tvt,
                            const CUtensorMap& to, const Fp8Args& a, cudaStream_t stream) {
     const size_t smem = sizeof(Fp8Smem) + 1024;
-    cudaError_t e = cudaFuncSetAttribute(fa_fwd_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    cudaError_t e = smem_limit_once<fa_fwd_fp8_kernel>(static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     const unsigned grid = static_cast<unsigned>(a.n_qblk) * static_cast<unsigned>(a.BH);
     fa_fwd_fp8_kernel<<<grid, kThreads, smem, stream>>>(tq, tk, tvt, to, a);

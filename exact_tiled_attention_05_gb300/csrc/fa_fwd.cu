@@ -826,9 +826,7 @@ cudaError_t launch_fwd_cap(unsigned grid, const CUtensorMap& tq, const CUtensorM
                            const CUtensorMap& tv, const CUtensorMap& to, const FwdArgs& args,
                            const FwdSched<Cap>& sc, cudaStream_t stream) {
     const size_t smem = sizeof(FwdSmem<HD>) + 1024;
-    cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<HD, Cap>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    cudaError_t e = smem_limit_once<fa_fwd_kernel<HD, Cap>>(static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     fa_fwd_kernel<HD, Cap><<<grid, kThreads, smem, stream>>>(tq, tk, tv, to, args, sc);
     return cudaGetLastError();

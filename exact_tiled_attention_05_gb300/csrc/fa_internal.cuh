@@ -2,6 +2,7 @@
 // host API (fa_api.cu) and the kernel translation units.
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <cuda.h>
@@ -120,6 +121,8 @@ struct BwdArgs {
     float scale;
     float scale_log2;
     int* status;
+    int zero_counters;   // prep: zero both work counters (inside fa_bwd)
+    int counters_zeroed; // dK/dV and dQ kernels: the prep before them zeroed the counters
 };
 
 // FP8 forward (d = 128).  The quantizer reads q, k, v and fills the FP8
@@ -162,6 +165,22 @@ struct TensorMaps3 {
 // B, H, N >= 1, causal 0 or 1, scale finite and > 0 (kErrInvalidArg); d 64 or
 // 128 (kErrUnsupported); B*H*N*d < 2^31 (kErrInvalidArg).  Defined in fa_api.cu.
 int check_shape(int B, int H, int N, int d, float scale, int causal);
+
+// Raises a kernel's dynamic shared-memory limit (cudaFuncSetAttribute) the
+// first time it is launched on a device, not before every launch.  Kernel: the
+// __global__ function (one counter per kernel instance and device).
+template <auto Kernel>
+cudaError_t smem_limit_once(int bytes) {
+    static std::atomic<int> set_on[64];  // per device: the limit already set, 0 = none
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64 && set_on[dev].load(std::memory_order_acquire) >= bytes)
+        return cudaSuccess;
+    e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && dev >= 0 && dev < 64) set_on[dev].store(bytes, std::memory_order_release);
+    return e;
+}
 
 // Launchers (defined in the kernel translation units).  Return a cudaError_t.
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,

@@ -89,6 +89,17 @@ def make_inputs(w: Workload, device="cpu", B=None, H=None, N=None, d=None, seed=
     return {n: t.to(device) for n, t in out.items()}
 
 
+def make_inputs_device(B, H, N, d, seed, device, backward=True):
+    """Q, K, V (and dO) as iid N(0, 1) bf16 [B, H, N, d], drawn by PyTorch's
+    generator on ``device`` (seeded, in that order): for sizes near the 2^31
+    element limit, where the host generator of make_inputs would take minutes.
+    The same recipe otherwise; the values differ from make_inputs' for a seed."""
+    g = torch.Generator(device=device).manual_seed(seed)
+    names = ("q", "k", "v", "do") if backward else ("q", "k", "v")
+    return {n: torch.randn((B, H, N, d), generator=g, device=device, dtype=torch.float32)
+            .to(torch.bfloat16) for n in names}
+
+
 def random_bf16(shape, seed: int, scale: float = 1.0, device="cpu"):
     """One bf16 tensor of iid N(0, scale^2) values from a seeded CPU generator."""
     g = torch.Generator(device="cpu").manual_seed(seed)

@@ -93,6 +93,7 @@ def test_fwd_argument_errors(lib):
     assert call(d=96) == fa.FA_ERR_UNSUPPORTED
     assert call(d=256) == fa.FA_ERR_UNSUPPORTED
     assert call(B=1 << 12, H=1 << 12, N=1 << 8) == fa.FA_ERR_INVALID_ARG  # >= 2^31 elements
+    assert call(B=1, H=16, N=1 << 20, d=128) == fa.FA_ERR_INVALID_ARG  # exactly 2^31 elements
     assert call(q=FAKE + 8) == fa.FA_ERR_MISALIGNED
     assert call(o=FAKE + 2) == fa.FA_ERR_MISALIGNED
     assert call(lse=FAKE + 2) == fa.FA_ERR_MISALIGNED

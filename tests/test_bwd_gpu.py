@@ -317,6 +317,37 @@ def test_long_sequence_non_causal_key_rows():
     check_grad(take(dv, krows), g[2], "dv sampled key rows N=2^15")
 
 
+def test_largest_accepted_size():
+    """The largest inputs the boundary takes: B·H·N·d = 16 · (2^20 - 64) · 128 =
+    2^31 - 2^17 elements (2^31 is refused), causal, with a ragged last tile.
+    Forward O and lse and backward dQ on 16 seeded rows of the first and the
+    last head (rows 0 and N - 1 among them) against the oracle, element by
+    element; on every head the identities sum_j dK_j = 0 and
+    sum_j dV_j = sum_i dO_i, summed in fp64 on the device."""
+    B, H, N, d = 1, 16, (1 << 20) - 64, 128
+    assert B * H * N * d < (1 << 31) <= B * H * (N + 64) * d
+    scale = 1.0 / math.sqrt(d)
+    inp = wl.make_inputs_device(B, H, N, d, seed=7000, device=DEV)
+    o, lse, dq, dk, dv = gpu_fwd_bwd(inp, True, scale)
+    heads = [0, H - 1]
+    rows = sampled_key_rows(N, len(heads), 16, 0, seed=7100)
+    sel = lambda t: bits(t[:, heads])
+    take = lambda t, width: np.stack([to_np(t.reshape(B * H, N, width)[h][torch.as_tensor(r, device=DEV)])
+                                      for h, r in zip(heads, rows)])
+    o_ref, l_ref = oracle.fwd_rows(sel(inp["q"]), sel(inp["k"]), sel(inp["v"]), scale, True, rows)
+    check_o(take(o, d), o_ref, "largest size O")
+    check_lse(take(lse, 1)[..., 0], l_ref, "largest size lse")
+    g = oracle.bwd_rows(sel(inp["q"]), sel(inp["k"]), sel(inp["v"]), sel(inp["do"]), scale, True,
+                        qrows=rows)
+    check_grad(take(dq, d), g[0], "largest size dq")
+    sk = (torch.sum(dk, dim=2, dtype=torch.float64).abs() /
+          torch.sum(dk.abs(), dim=2, dtype=torch.float64).clamp_min(1e-30))
+    assert sk.max().item() <= 1e-2, f"sum_j dK_j not ~0: {sk.max().item()}"
+    sv = ((torch.sum(dv, dim=2, dtype=torch.float64) - torch.sum(inp["do"], dim=2, dtype=torch.float64)).abs() /
+          torch.sum(dv.abs(), dim=2, dtype=torch.float64).clamp_min(1e-30))
+    assert sv.max().item() <= 1e-2, f"sum_j dV_j != sum_i dO_i: {sv.max().item()}"
+
+
 def test_backward_bitwise_repeatable_back_to_back():
     """16 forward + backward passes of the fwd+bwd workload enqueued back to back
     on one stream (fresh output buffers each, no host synchronisation between

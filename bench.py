@@ -191,6 +191,44 @@ def oracle_baseline(w, inputs_cpu, target_s=12.0, max_heads=64):
                       f"{spent:.1f} s on {threads} host threads"}
 
 
+def oracle_forward_rates(threads, budget_s=1.0):
+    """The fp64 oracle's forward beside the other four workloads: per workload and
+    mask, seeded query rows of one head (all rows of the 256-row head), adding rows
+    until a call takes about `budget_s` seconds (calls on the 256-row head are
+    repeated to fill it); on every host thread and, for the two small workloads,
+    on one thread too.  FLOPs are those of the rows evaluated (4·d per visible
+    key, so causal rows count only their own keys)."""
+    import numpy as np
+    import oracle
+    from exact_tiled_attention_05_gb300 import workloads as wl
+    out = {}
+    for name in ("single_head_256", "fwd_2k_d64", "fwd_8k_d128_kx3", "fwd_32k_d128"):
+        w = wl.WORKLOADS[name]
+        inp = wl.make_inputs(w, B=1, H=1)
+        b = {n: wl.bf16_bits(inp[n]) for n in ("q", "k", "v")}
+        for causal in w.causal_modes:
+            for nt in ((threads, 1) if w.N <= 2048 else (threads,)):
+                count = min(16, w.N)
+                while True:
+                    rows = wl.sampled_rows(w, count=count, BH=1, N=w.N)
+                    reps, spent = 0, 0.0
+                    while spent < budget_s and (reps == 0 or count == w.N):
+                        t0 = time.perf_counter()
+                        oracle.fwd_rows(b["q"], b["k"], b["v"], w.scale, causal, rows, nthreads=nt)
+                        spent += time.perf_counter() - t0
+                        reps += 1
+                    if spent >= budget_s / 2 or count == w.N:
+                        break
+                    count = min(w.N, count * 4)
+                keys = (rows[0] + 1) if causal else np.full(rows.shape[1], w.N)
+                flops = 4.0 * w.d * float(keys.sum()) * reps
+                mode = "causal" if causal else "non-causal"
+                out[f"{name} {mode}, {nt} thread{'s' if nt > 1 else ''}"] = {
+                    "gflops": flops / spent / 1e9, "rows": int(rows.shape[1]), "calls": reps,
+                    "seconds": round(spent, 3)}
+    return out
+
+
 def run_reference(args, world, rank):
     """--impl reference: the oracle on the host cores, same metric and config."""
     from exact_tiled_attention_05_gb300 import workloads as wl
@@ -528,6 +566,7 @@ def run_gpu(args, world, rank, local):
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = oracle_baseline(w, cpu_in)
+        line["oracle_forward_rates"] = oracle_forward_rates(line["cpu_baseline"]["cores"])
     if rank == 0:
         print(json.dumps(line), flush=True)
 

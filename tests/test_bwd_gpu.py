@@ -264,7 +264,7 @@ def sampled_key_rows(N, BH, count, lo, seed):
     return np.array(out, dtype=np.int64)
 
 
-@pytest.mark.parametrize("d,causal", [(128, True), (64, False)])
+@pytest.mark.parametrize("d,causal", [(128, True), (64, False), (64, True), (128, False)])
 def test_long_sequence_sampled_rows_and_invariants(d, causal):
     """N = 2^17 (1024 key and query tiles per head).  Element by element against
     the oracle's sampled-row backward: dQ on 64 seeded query rows per head (rows
@@ -277,12 +277,12 @@ def test_long_sequence_sampled_rows_and_invariants(d, causal):
     sums to one)."""
     B, H, N = 1, 2, 1 << 17
     scale = 1.0 / math.sqrt(d)
-    inp = small_inputs(B, H, N, d, seed=5000 + d)
+    inp = small_inputs(B, H, N, d, seed=5000 + d + causal)
     _, _, dq, dk, dv = gpu_fwd_bwd(inp, causal, scale)
     dq_n = to_np(dq).reshape(B * H, N, d)
     dk_n = to_np(dk).reshape(B * H, N, d)
     dv_n = to_np(dv).reshape(B * H, N, d)
-    qrows = sampled_key_rows(N, B * H, 64, 0, seed=6000 + d)
+    qrows = sampled_key_rows(N, B * H, 64, 0, seed=6000 + d + causal)
     krows = sampled_key_rows(N, B * H, 32, N - 8192, seed=6100 + d) if causal else None
     g = oracle.bwd_rows(bits(inp["q"]), bits(inp["k"]), bits(inp["v"]), bits(inp["do"]), scale,
                         causal, qrows=qrows, krows=krows)

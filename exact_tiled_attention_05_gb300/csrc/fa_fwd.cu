@@ -585,25 +585,21 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
             bool rescale = false;
             float alphaA = 1.f, alphaB = 1.f;
             {
+                // without branches (selects and multiplications by 1 where nothing
+                // moves; fewer instructions than divergent branches): m = -inf,
+                // before the first tile, takes the tile's max without a rescale
                 const float mxA = pmA * sl2, mxB = pmB * sl2;
-                if (mA == -INFINITY) {
-                    mA = mxA;
-                } else if (mxA > mA + kRescaleThreshold) {
-                    rescale = true;
-                    alphaA = ex2(mA - mxA);
-                    lA = f2_mul(lA, f2_pack(alphaA, alphaA));
-                    lcA *= alphaA;
-                    mA = mxA;
-                }
-                if (mB == -INFINITY) {
-                    mB = mxB;
-                } else if (mxB > mB + kRescaleThreshold) {
-                    rescale = true;
-                    alphaB = ex2(mB - mxB);
-                    lB = f2_mul(lB, f2_pack(alphaB, alphaB));
-                    lcB *= alphaB;
-                    mB = mxB;
-                }
+                const bool upA = mxA > mA + kRescaleThreshold, upB = mxB > mB + kRescaleThreshold;
+                const bool rsA = upA && mA != -INFINITY, rsB = upB && mB != -INFINITY;
+                alphaA = rsA ? ex2(mA - mxA) : 1.f;
+                alphaB = rsB ? ex2(mB - mxB) : 1.f;
+                lA = f2_mul(lA, f2_pack(alphaA, alphaA));
+                lB = f2_mul(lB, f2_pack(alphaB, alphaB));
+                lcA *= alphaA;
+                lcB *= alphaB;
+                mA = upA ? mxA : mA;
+                mB = upB ? mxB : mB;
+                rescale = rsA || rsB;
             }
             const float negA = (mA == -INFINITY) ? 0.f : -mA;
             const float negB = (mB == -INFINITY) ? 0.f : -mB;

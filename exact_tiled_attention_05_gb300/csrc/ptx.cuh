@@ -401,9 +401,12 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 
 // Bounded wait by every lane of a warp, with one verdict for the whole warp.
 // (Every lane polls: letting one lane poll and broadcast measured slower, as
-// the extra shuffle sits on the softmax critical path.)
+// the extra shuffle sits on the softmax critical path.)  The first poll is
+// voted on at once, so a barrier that has already completed costs a poll, a
+// vote and a uniform branch, without the per-lane wait loop.
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
                                                const volatile int* abort) {
+    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;  // warp-uniform fast path
     const bool ok = mbar_wait(bar, parity, timeout_ns, abort);
     return __all_sync(0xffffffffu, ok);
 }

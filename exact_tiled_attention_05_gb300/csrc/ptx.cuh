@@ -401,14 +401,20 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 
 // Bounded wait by every lane of a warp, with one verdict for the whole warp.
 // (Every lane polls: letting one lane poll and broadcast measured slower, as
-// the extra shuffle sits on the softmax critical path.)  The first poll is
-// voted on at once, so a barrier that has already completed costs a poll, a
-// vote and a uniform branch, without the per-lane wait loop.
+// the extra shuffle sits on the softmax critical path.)  Every poll is voted
+// on, so the warp's control flow stays uniform: a barrier that has already
+// completed costs a poll, a vote and a uniform branch, and a timeout or abort
+// seen by any lane ends the wait for all of them.
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
                                                const volatile int* abort) {
     if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;  // warp-uniform fast path
-    const bool ok = mbar_wait(bar, parity, timeout_ns, abort);
-    return __all_sync(0xffffffffu, ok);
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+        if ((it & 63u) == 0u &&
+            __any_sync(0xffffffffu, *abort != 0 || globaltimer_ns() - t0 > timeout_ns))
+            return false;
+    }
 }
 
 __device__ __forceinline__ float ex2(float x) {

@@ -74,6 +74,21 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
     return r;
 }
 
+// Four floats -> four E4M3 codes in one word, a0 in the lowest byte (the two
+// conversions write the two halves of the word).
+__device__ __forceinline__ uint32_t e4m3x4(float a0, float a1, float a2, float a3) {
+    uint32_t r;
+    asm("{\n"
+        " .reg .b16 lo, hi;\n"
+        " cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n"
+        " cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n"
+        " mov.b32 %0, {lo, hi};\n"
+        "}"
+        : "=r"(r)
+        : "f"(a0), "f"(a1), "f"(a2), "f"(a3));
+    return r;
+}
+
 // x rounded to E4M3 (as the packing above rounds it) and back to fp32.
 __device__ __forceinline__ float e4m3_round(float x) {
     const uint16_t c = static_cast<uint16_t>(e4m3x2(x, 0.f));
@@ -670,23 +685,27 @@ fa_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 // chunk of row x: repetitions 8hh .. 8hh + 7, an E4M3 pair each
                 uint32_t w[2][4];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
+                for (int i2 = 0; i2 < 4; ++i2) {
+                    float pv[2][2][2];  // [repetition 2 i2 + ii][row x][pair element]
 #pragma unroll
-                    for (int x = 0; x < 2; ++x) {
-                        const int e = hh * 32 + 4 * i + 2 * x;
-                        const uint64_t x2 = f2_fma(f2_pack_u(SR(e), SR(e + 1)), sl2_pair, x == 0 ? negA2 : negB2);
-                        const float2 xv = f2_unpack(x2);
-                        const float p0 = ex2(xv.x), p1 = ex2(xv.y);
-                        if (x == 0)
-                            tA = f2_add(tA, f2_pack(p0, p1));
-                        else
-                            tB = f2_add(tB, f2_pack(p0, p1));
-                        const uint32_t pr = e4m3x2(p0, p1);
-                        if (i & 1)
-                            w[x][i >> 1] |= pr << 16;
-                        else
-                            w[x][i >> 1] = pr;
+                    for (int ii = 0; ii < 2; ++ii) {
+#pragma unroll
+                        for (int x = 0; x < 2; ++x) {
+                            const int e = hh * 32 + 4 * (2 * i2 + ii) + 2 * x;
+                            const uint64_t x2 = f2_fma(f2_pack_u(SR(e), SR(e + 1)), sl2_pair, x == 0 ? negA2 : negB2);
+                            const float2 xv = f2_unpack(x2);
+                            const float p0 = ex2(xv.x), p1 = ex2(xv.y);
+                            if (x == 0)
+                                tA = f2_add(tA, f2_pack(p0, p1));
+                            else
+                                tB = f2_add(tB, f2_pack(p0, p1));
+                            pv[ii][x][0] = p0;
+                            pv[ii][x][1] = p1;
+                        }
                     }
+#pragma unroll
+                    for (int x = 0; x < 2; ++x)
+                        w[x][i2] = e4m3x4(pv[0][x][0], pv[0][x][1], pv[1][x][0], pv[1][x][1]);
                 }
                 st_shared_v4(pbuf + p_row_A + p_chunk[hh], w[0][0], w[0][1], w[0][2], w[0][3]);
                 st_shared_v4(pbuf + p_row_B + p_chunk[hh], w[1][0], w[1][1], w[1][2], w[1][3]);
